@@ -1,0 +1,223 @@
+/*
+ * moe.h -- C ABI of libmoe.so: a single-GPU MoE layer for GB300 (sm_103a).
+ *
+ * The layer is the compute chain of the token-level dispatcher described in
+ * "MoE Parallel Folding: Heterogeneous Parallelism Mappings for Efficient
+ * Large-Scale MoE Model Training with Megatron Core" (arXiv 2504.14960),
+ * study notes, "method overview": the router gives each token its Top-K
+ * experts, a permutation makes each expert's tokens contiguous, the experts'
+ * FFN runs, an un-permutation restores the token order; the backward runs the
+ * same chain in reverse. The exchanges between ranks in that chain
+ * (All-to-All-V, AllGather-V, ReduceScatter-V) are absent: one GPU holds every
+ * expert, so each exchange is the identity.
+ *
+ * Conventions for every call below
+ *  - Ownership: the caller allocates and owns every buffer. All tensor
+ *    pointers are DEVICE pointers, 16-byte aligned, dense row-major with the
+ *    layout stated. The library allocates nothing on the calls below.
+ *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream). No call synchronises the host or copies data
+ *    to the host, except moe_get_status.
+ *  - Data-dependent sizes stay on the device: the number of kept assignments
+ *    and the per-expert row counts are read by later kernels from `offsets`.
+ *    Buffers indexed by permuted row are sized for the worst case T*K rows.
+ *  - Errors: argument checks that fail return MOE_ERR_INVALID_ARG or
+ *    MOE_ERR_UNSUPPORTED before anything is launched; a failed launch returns
+ *    MOE_ERR_CUDA. Device-side failures (a bounded wait that gave up, an index
+ *    out of range) are recorded in the status word inside `ws` and read with
+ *    moe_get_status; the kernel that saw one skips the bad access and returns.
+ *  - Determinism: every output is bitwise reproducible from run to run.
+ *  - dtype: MOE_BF16 means x, weights and activations are bf16 (accumulation
+ *    in fp32); MOE_F32 means all of them are fp32. Logits, probabilities,
+ *    combine weights, dXp, dx and every weight gradient are fp32 in both.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad pointer, size or alignment                    */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but a shape this build has no kernel for   */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed               */
+  MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (status word only)  */
+  MOE_ERR_DEVICE = 5       /* device: an index check failed (status word only)   */
+} moe_status_t;
+
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+
+typedef void *moe_stream_t; /* a cudaStream_t */
+
+/* The problem statement of one MoE layer (study notes, "prerequisites":
+ * Top-K gating and the capacity factor; "method overview" and "key modules":
+ * drop and dropless routing, sub-sequence dropping).                          */
+typedef struct {
+  int64_t T;               /* tokens (micro-batch x sequence, flattened)      */
+  int32_t d;               /* hidden size                                    */
+  int32_t E;               /* routed experts, 1..64                          */
+  int32_t K;               /* Top-K, 1..min(E, 8)                            */
+  int32_t F;               /* routed expert SwiGLU intermediate size         */
+  int32_t dtype;           /* MOE_BF16 or MOE_F32                            */
+  int32_t drop;            /* 0 dropless, 1 capacity-factor dropping         */
+  float capacity_factor;   /* CF, > 0 (used when drop = 1)                   */
+  int64_t subseq_len;      /* S: drops are decided per block of S tokens of
+                              the flat order; 0 means S = T (full sequence)  */
+  int32_t renorm;          /* 1: combine weights renormalised over the K     */
+  int32_t Fs;              /* shared expert SwiGLU size, 0 = none            */
+} moe_shape_t;
+
+/* Library version, "major.minor.patch". */
+const char *moe_version(void);
+
+/* Human-readable name of a status code. */
+const char *moe_status_string(moe_status_t s);
+
+/* Bytes of device workspace `ws` that the calls taking a `ws` need for this
+ * shape (a multiple of 256; the caller allocates it 256-byte aligned and may
+ * reuse it across calls on one stream). Returns 0 for an invalid shape. */
+size_t moe_workspace_size(const moe_shape_t *shape);
+
+/* Clears the device status word in `ws` (asynchronous). */
+moe_status_t moe_clear_status(void *ws, moe_stream_t stream);
+
+/* Synchronises `stream`, then returns the first device-side error recorded
+ * in `ws` since the last moe_clear_status (MOE_OK if none). *info, if not
+ * NULL, receives a kernel-specific detail word. */
+moe_status_t moe_get_status(void *ws, moe_stream_t stream, uint32_t *info);
+
+/* ---- forward ------------------------------------------------------------ */
+
+/* Router: logits, softmax, Top-K, combine weights, capacity dropping.
+ * Study notes, "method overview" (router Top-K), "prerequisites" (Top-K
+ * gating, capacity factor), "key modules" and the quote of the paper's
+ * section 3.3 (sub-sequence dropping is the default drop rule).
+ *   x [T,d] dtype; W_r [E,d] dtype; b_r [E] fp32 or NULL (added to logits);
+ *   w_sg [d] dtype or NULL: shared-expert gate vector;
+ *   out: logits [T,E] fp32 = x W_r^T (+ b_r), accumulated in fp32;
+ *        gate_logit [T] fp32 = x . w_sg (NULL iff w_sg is NULL);
+ *        topk_idx [T,K] int32, topk_prob [T,K] fp32, topk_w [T,K] fp32,
+ *        keep [T,K] uint8: as moe_route_topk.
+ *   ws: workspace of moe_workspace_size(shape) bytes.                        */
+moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
+                       const float *b_r, const void *w_sg, float *logits,
+                       float *gate_logit, int32_t *topk_idx, float *topk_prob,
+                       float *topk_w, uint8_t *keep, void *ws, moe_stream_t stream);
+
+/* Top-K gating and capacity dropping from caller-supplied fp32 logits [T,E].
+ * p = softmax(logits) computed in fp32 with a fixed operation order (own exp:
+ * Cody-Waite reduction and degree-7 Taylor; pairwise sum; IEEE division).
+ * topk_idx: K arg-max rounds over p, ties to the lower expert index, in
+ * selection order; topk_prob = p at those experts; topk_w = topk_prob / Z with
+ * Z = sum over the K slots in slot order (renorm = 1) or topk_prob (renorm 0).
+ * keep[t,k] = 1 unless drop = 1 and the assignment is not among the
+ * ceil(CF*S_j*K/E) highest-probability assignments of its (sub-sequence,
+ * expert), ties to the lower token index. Kept weights are not renormalised
+ * again after a drop.                                                        */
+moe_status_t moe_route_topk(const moe_shape_t *shape, const float *logits,
+                            int32_t *topk_idx, float *topk_prob, float *topk_w,
+                            uint8_t *keep, void *ws, moe_stream_t stream);
+
+/* Permutation map and row copy (study notes, "method overview": the
+ * permutation makes each expert's tokens contiguous).
+ *   in:  x [T,d] dtype; topk_idx, keep [T,K].
+ *   out: counts [E] int32 (kept assignments per expert); offsets [E+1] int32
+ *        (exclusive prefix of counts; offsets[E] = n_kept);
+ *        row_of [T,K] int32: permuted row of each assignment, -1 if dropped;
+ *        src_of [T*K] int32: t*K+k of each permuted row (first n_kept valid);
+ *        Xp [T*K, d] dtype: Xp[row_of[t,k]] = x[t]; rows are expert-major and
+ *        token-ascending inside an expert; rows >= n_kept are not written.  */
+moe_status_t moe_permute(const moe_shape_t *shape, const void *x,
+                         const int32_t *topk_idx, const uint8_t *keep, void *Xp,
+                         int32_t *row_of, int32_t *src_of, int32_t *counts,
+                         int32_t *offsets, void *ws, moe_stream_t stream);
+
+/* Grouped SwiGLU FFN (study notes, "method overview": expert FFN
+ * computation). Group g owns rows [offsets[g], offsets[g+1]) of Xp.
+ *   dtype: MOE_BF16 (tcgen05 tensor-core path) or MOE_F32;
+ *   max_rows: rows allocated in Xp/A_save/H_save/Yp (offsets[n_groups] must
+ *   not exceed it); d, F as in moe_shape_t; n_groups: experts (1 for a shared
+ *   expert with offsets = {0, T}).
+ *   W_gu [n_groups, 2F, d] (rows [0,F) gate, [F,2F) up); W_down [n_groups,d,F].
+ *   out: A_save [max_rows, 2F] = [G|U] (NULL: not stored; the backward needs
+ *        it); H_save [max_rows, F] = silu(G)*U (required: it is also the
+ *        input of the down projection); Yp [max_rows, d] = H W_down^T.
+ *        Only rows < offsets[n_groups] are written.
+ *   ws: any workspace of this library (only its status word is used).
+ *   bf16 requires d % 128 == 0 and F % 128 == 0 (else MOE_ERR_UNSUPPORTED);
+ *   fp32 requires d % 4 == 0.                                                */
+moe_status_t moe_expert_ffn(int32_t dtype, int64_t max_rows, int32_t d, int32_t F,
+                            int32_t n_groups, const int32_t *offsets, const void *Xp,
+                            const void *W_gu, const void *W_down, void *A_save,
+                            void *H_save, void *Yp, void *ws, moe_stream_t stream);
+
+/* Un-permutation with the weighted Top-K combine (study notes, "method
+ * overview": the un-permutation restores the original token order).
+ *   out[t] = sum over kept slots k, in slot order, of topk_w[t,k] *
+ *   Yp[row_of[t,k]] (+ sigmoid(gate_logit[t]) * Ys[t]), summed in fp32 and
+ *   stored once in dtype. Ys [T,d] and gate_logit [T] are both NULL or both
+ *   set. A token with every slot dropped and no shared expert outputs 0.     */
+moe_status_t moe_unpermute(const moe_shape_t *shape, const void *Yp,
+                           const int32_t *row_of, const float *topk_w, const void *Ys,
+                           const float *gate_logit, void *out, moe_stream_t stream);
+
+/* ---- backward (study notes, "method overview": the backward runs the
+ *      chain in reverse) -------------------------------------------------- */
+
+/* dYp[row_of[t,k]] = dtype(topk_w[t,k] * dout[t]) for kept slots;
+ * dw[t,k] = <dout[t], Yp[row_of[t,k]]> fp32 (0 when dropped);
+ * with a shared expert: dYs[t] = dtype(s_t * dout[t]), dz[t] = s_t (1 - s_t)
+ * <dout[t], Ys[t]> with s_t = sigmoid(gate_logit[t]). Ys, gate_logit, dYs, dz
+ * are all NULL or all set.                                                  */
+moe_status_t moe_unpermute_bwd(const moe_shape_t *shape, const void *dout,
+                               const void *Yp, const int32_t *row_of,
+                               const float *topk_w, const void *Ys,
+                               const float *gate_logit, void *dYp, float *dw,
+                               void *dYs, float *dz, moe_stream_t stream);
+
+/* Backward of moe_expert_ffn (same argument meanings).
+ *   in:  dYp [max_rows,d] dtype; Xp; A_save; H_save; W_gu; W_down.
+ *   out: dXp [max_rows, d] fp32 = dA W_gu; dW_gu [n_groups,2F,d] fp32 =
+ *        dA^T Xp; dW_down [n_groups,d,F] fp32 = dYp^T H (zero for a group
+ *        with no rows);
+ *   dA [max_rows, 2F] dtype: caller-owned buffer that receives
+ *   [dG | dU] = [dH*U*sg*(1+G(1-sg)) | dH*G*sg], dH = dYp W_down,
+ *   sg = sigmoid(G), G|U from A_save.                                        */
+moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int32_t F,
+                                int32_t n_groups, const int32_t *offsets,
+                                const void *dYp, const void *Xp, const void *A_save,
+                                const void *H_save, const void *W_gu,
+                                const void *W_down, void *dA, float *dXp,
+                                float *dW_gu, float *dW_down, void *ws,
+                                moe_stream_t stream);
+
+/* dx[t] = sum over kept slots of dXp[row_of[t,k]] (+ dx_add[t]), fp32.
+ * dXp [T*K,d] fp32; dx_add [T,d] fp32 or NULL; dx [T,d] fp32.               */
+moe_status_t moe_permute_bwd(const moe_shape_t *shape, const float *dXp,
+                             const int32_t *row_of, const float *dx_add, float *dx,
+                             moe_stream_t stream);
+
+/* Router backward. g = dw [T,K]; renorm: dp_j = (g_j - sum_k g_k w_k) / Z on
+ * the Top-K (Z = sum of topk_prob), else dp = g there; dp = 0 elsewhere;
+ * p = softmax(logits) as in moe_route_topk; dl_i = p_i (dp_i - sum_j p_j dp_j).
+ *   out: dW_r [E,d] fp32 = dl^T x; db_r [E] fp32 = sum_t dl (NULL: skipped);
+ *        dx_router [T,d] fp32 = (dx_in or 0) + dl W_r (+ dz w_sg);
+ *        dw_sg [d] fp32 = dz^T x (NULL iff dz is NULL).
+ *   w_sg, dz, dw_sg: all NULL or all set. dx_in [T,d] fp32 or NULL.        */
+moe_status_t moe_route_bwd(const moe_shape_t *shape, const void *x, const void *W_r,
+                           const void *w_sg, const float *logits,
+                           const int32_t *topk_idx, const float *topk_prob,
+                           const float *topk_w, const float *dw, const float *dz,
+                           const float *dx_in, float *dW_r, float *db_r,
+                           float *dw_sg, float *dx_router, void *ws,
+                           moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

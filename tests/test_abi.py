@@ -1,0 +1,83 @@
+"""The C ABI without a GPU: libmoe.so loads, exports every entry point that
+include/moe.h declares, sizes workspaces, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from token_dispatch_expert_moe_gb300 import build
+    if not os.path.exists(build.LIB):
+        build.build()
+    from token_dispatch_expert_moe_gb300 import _lib
+    return _lib
+
+
+def _declared():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"\b(moe_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared()
+    assert "moe_route" in declared and "moe_expert_ffn_bwd" in declared
+    for name in declared:
+        assert hasattr(L.lib, name), name
+    assert set(declared) == set(L.EXPORTED)
+
+
+def test_version_and_status_strings(L):
+    assert L.version().count(".") == 2
+    for code in range(6):
+        assert L.lib.moe_status_string(code)
+
+
+def test_workspace_size(L):
+    from synthetic import CONFIGS
+    for cfg in CONFIGS.values():
+        n = L.moe_workspace_size(L.shape_of(cfg))
+        assert n > 0 and n % 256 == 0
+    bad = L.MoEShape(T=10, d=64, E=65, K=2, F=128, dtype=1)
+    assert L.moe_workspace_size(bad) == 0
+    bad = L.MoEShape(T=10, d=64, E=8, K=9, F=128, dtype=1)
+    assert L.moe_workspace_size(bad) == 0
+    bad = L.MoEShape(T=10, d=60, E=8, K=2, F=128, dtype=1)   # d % 8 for bf16
+    assert L.moe_workspace_size(bad) == 0
+
+
+def test_invalid_arguments_rejected_on_host(L):
+    s = L.MoEShape(T=16, d=64, E=4, K=2, F=128, dtype=1)
+    fake = 1 << 20   # never dereferenced: validation fails first
+    with pytest.raises(L.MoEError) as e:
+        L.moe_route(s, None, fake, None, None, fake, None, fake, fake, fake, fake, fake, 0)
+    assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:   # misaligned x
+        L.moe_route(s, fake + 2, fake, None, None, fake, None, fake, fake, fake, fake, fake, 0)
+    assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:   # w_sg without gate_logit
+        L.moe_route(s, fake, fake, None, fake, fake, None, fake, fake, fake, fake, fake, 0)
+    assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:   # bf16 FFN needs d, F multiples of 128
+        L.moe_expert_ffn(1, 32, 96, 128, 4, fake, fake, fake, fake, None, fake, fake, fake, 0)
+    assert e.value.code == 2
+    with pytest.raises(L.MoEError) as e:   # H_save is required
+        L.moe_expert_ffn(1, 32, 128, 128, 4, fake, fake, fake, fake, None, None, fake, fake, 0)
+    assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:   # unpermute: Ys without gate_logit
+        L.moe_unpermute(s, fake, fake, fake, fake, None, fake, 0)
+    assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:
+        L.moe_route_bwd(s, fake, fake, fake, fake, fake, fake, fake, fake, None, None, fake, None,
+                        None, fake, fake, 0)
+    assert e.value.code == 1

@@ -1,0 +1,669 @@
+// Grouped GEMMs of the SwiGLU experts on the sm_103a tensor cores.
+//
+// MoE Parallel Folding (arXiv 2504.14960) study notes, "method overview":
+// after the permutation each expert's tokens are contiguous and the experts'
+// FFN runs on them; the backward runs the same chain in reverse. The expert
+// rows of group g are [offsets[g], offsets[g+1]) of the permuted buffers;
+// offsets stay on the device and every CTA derives the tile list from them.
+//
+// One persistent, warp-specialised kernel template, one CTA per SM:
+//   warp 0      TMA producer: 128B-swizzled boxes into a 4-stage smem ring;
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
+//               fp32 accumulate), M = 128, N = 128..256, K = 16 per
+//               instruction, 4 per 64-deep stage; tcgen05.commit frees the
+//               stage and, at the end of a tile, hands the accumulator over;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
+//               quarter per warp), fused math, stores to global memory.
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
+// the mainloop of the next.
+//
+// The six GEMMs (A: M x K, B: N x K, per group g):
+//   GU      [G|U] = Xp W_gu[g]^T, SwiGLU epilogue H = silu(G) U (+ A_save)
+//   DOWN    Yp    = H W_down[g]^T
+//   DH      dH    = dYp W_down[g]  -> epilogue dA = [dG | dU]   (B MN-major)
+//   DX      dXp   = dA W_gu[g]                                   (B MN-major)
+//   WGD     dW_down[g] = dYp_g^T H_g     (K = the group's rows; A, B MN-major)
+//   WGU     dW_gu[g]   = dA_g^T Xp_g
+// In GU/DOWN/DH/DX a tile's rows past the group's end belong to the next
+// group (or are zero-filled past the buffer); only their outputs are masked.
+// In WGD/WGU the reduction runs over the group's rows, so K rows past the end
+// are zeroed in shared memory before the MMA reads them.
+//
+// Every wait on an mbarrier is bounded (about two seconds of
+// %globaltimer); on expiry the kernel records MOE_ERR_TIMEOUT in the status
+// word, tells the other roles to stop, drains what it has in flight and
+// returns, so the GPU context stays usable.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+enum Mode { GU = 0, DOWN = 1, DH = 2, DX = 3, WGD = 4, WGU = 5 };
+
+constexpr int kStages = 4;
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kABytes = BM * BK * 2;          // 16 KB
+constexpr int kBBytesMax = 256 * BK * 2;      // 32 KB
+constexpr int kStageBytes = kABytes + kBBytesMax;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct TcParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  int mode;
+  int n_groups;
+  int64_t max_rows;
+  int d, F;
+  int M_fixed;   // WGD/WGU: rows of the weight-gradient matrix
+  int N;         // output columns (GU: F, the MMA sees 2 x 128)
+  int K_fixed;   // GU/DOWN/DH/DX: reduction depth
+  int64_t b_group_rows;  // B rows per group in the B tensor map (y offset)
+  const int32_t *offsets;
+  void *out0;    // GU: H; DOWN: Yp; DH: dA; DX: dXp; WG*: dW
+  void *out1;    // GU: A_save (nullable)
+  const void *aux;  // DH: A_save
+  uint32_t *status;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format):
+// start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
+// byte offset >> 4 in 32-45, descriptor version 1 at bit 46, layout
+// SWIZZLE_128B (2) in bits 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), A/B major-ness (bits 15, 16: 1 = MN-major),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int MODE> struct ModeTraits {
+  static constexpr bool red = (MODE == WGD || MODE == WGU);
+  static constexpr int a_mn = red ? 1 : 0;
+  static constexpr int b_mn = (MODE == DH || MODE == DX || red) ? 1 : 0;
+};
+
+struct SharedState {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+  int total_tiles;
+  int tile_start[65];  // ROWS mode: first tile index of each group
+  int mtiles[64];      // ROWS mode: m-tiles of each group
+};
+
+struct Tile {
+  int g, m, n;       // group, m-tile, n-tile
+  int row0, rows;    // ROWS: first row and row count of the group; RED: K rows
+};
+
+template <int MODE, int BN>
+__device__ __forceinline__ Tile decode_tile(const TcParams &p, const SharedState &st, int idx) {
+  Tile t;
+  if constexpr (ModeTraits<MODE>::red) {
+    const int MT = p.M_fixed / BM, NT = p.N / BN;
+    t.g = idx / (MT * NT);
+    const int loc = idx % (MT * NT);
+    t.n = loc / MT;
+    t.m = loc % MT;
+    t.row0 = p.offsets[t.g];
+    t.rows = p.offsets[t.g + 1] - t.row0;
+  } else {
+    int g = 0;
+    while (g + 1 < p.n_groups && st.tile_start[g + 1] <= idx) ++g;
+    const int loc = idx - st.tile_start[g];
+    const int mt = st.mtiles[g];
+    t.g = g;
+    t.n = loc / mt;
+    t.m = loc % mt;
+    t.row0 = p.offsets[g];
+    t.rows = p.offsets[g + 1] - t.row0;
+  }
+  return t;
+}
+
+__device__ bool wait_bounded(SharedState &st, uint32_t bar, uint32_t parity, uint32_t *status,
+                             uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (st.abort) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      report(status, MOE_ERR_TIMEOUT, kInfoGemmTimeout + role);
+      st.abort = 1;
+      return false;
+    }
+  }
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using TR = ModeTraits<MODE>;
+  constexpr int MMA_N = (MODE == GU) ? 256 : BN;
+  constexpr int B_BOXES = TR::b_mn ? MMA_N / 64 : MMA_N / 128;
+  constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
+  constexpr uint32_t kStageTx = kABytes + MMA_N * BK * 2;
+  constexpr uint32_t kIdesc = instr_desc(BM, MMA_N, TR::a_mn, TR::b_mn);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  SharedState &st = *reinterpret_cast<SharedState *>(smem + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- set-up: tile table, barriers, TMEM
+  if (threadIdx.x == 0) {
+    st.abort = 0;
+    int total = 0;
+    bool bad = false;
+    if constexpr (TR::red) {
+      for (int g = 0; g < p.n_groups; ++g)
+        if (p.offsets[g + 1] < p.offsets[g]) bad = true;
+      total = p.n_groups * (p.M_fixed / BM) * (p.N / BN);
+    } else {
+      const int NT = p.N / (MODE == GU ? 128 : BN);
+      for (int g = 0; g < p.n_groups; ++g) {
+        const int rows = p.offsets[g + 1] - p.offsets[g];
+        if (rows < 0) bad = true;
+        const int mt = rows > 0 ? (rows + BM - 1) / BM : 0;
+        st.tile_start[g] = total;
+        st.mtiles[g] = mt > 0 ? mt : 1;
+        total += mt * NT;
+      }
+      st.tile_start[p.n_groups] = total;
+    }
+    if (p.offsets[0] < 0 || (int64_t)p.offsets[p.n_groups] > p.max_rows) bad = true;
+    if (bad) {
+      report(p.status, MOE_ERR_DEVICE, kInfoOffsets);
+      total = 0;
+    }
+    st.total_tiles = total;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&st.full[s]), 1);
+      mbar_init(smem_u32(&st.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&st.tfull[b]), 1);
+      mbar_init(smem_u32(&st.tempty[b]), 4);
+    }
+    mbar_init(smem_u32(&st.drain), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&st.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = st.tmem_base;
+  const int total = st.total_tiles;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      int it = 0;
+      int last_phase[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+      for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x) {
+        const Tile t = decode_tile<MODE, BN>(p, st, ti);
+        const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 1)) break;
+          const uint32_t full = smem_u32(&st.full[s]);
+          mbar_expect_tx(full, kStageTx);
+          last_phase[s] = (int)ph;
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          if constexpr (TR::red) {
+            const int krow = t.row0 + kb * BK;
+#pragma unroll
+            for (int b = 0; b < A_BOXES; ++b)
+              tma_load_2d(sa + b * 8192, &p.tmA, full, t.m * BM + 64 * b, krow);
+#pragma unroll
+            for (int b = 0; b < B_BOXES; ++b)
+              tma_load_2d(sb + b * 8192, &p.tmB, full, t.n * BN + 64 * b, krow);
+          } else {
+            const int arow = t.row0 + t.m * BM;
+            tma_load_2d(sa, &p.tmA, full, kb * BK, arow);
+            const int64_t gb = (int64_t)t.g * p.b_group_rows;
+            if constexpr (MODE == GU) {
+              tma_load_2d(sb, &p.tmB, full, kb * BK, (int)(gb + t.n * 128));
+              tma_load_2d(sb + 16384, &p.tmB, full, kb * BK, (int)(gb + p.F + t.n * 128));
+            } else if constexpr (TR::b_mn) {
+#pragma unroll
+              for (int b = 0; b < B_BOXES; ++b)
+                tma_load_2d(sb + b * 8192, &p.tmB, full, t.n * BN + 64 * b, (int)(gb + kb * BK));
+            } else {
+#pragma unroll
+              for (int b = 0; b < B_BOXES; ++b)
+                tma_load_2d(sb + b * 16384, &p.tmB, full, kb * BK, (int)(gb + t.n * BN + 128 * b));
+            }
+          }
+        }
+      }
+      // drain: every issued load must land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (last_phase[s] >= 0) {
+          const uint32_t bar = smem_u32(&st.full[s]);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(bar, (uint32_t)last_phase[s]) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    int it = 0, tcount = 0;
+    bool issued_any = false;
+    for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x, ++tcount) {
+      const Tile t = decode_tile<MODE, BN>(p, st, ti);
+      const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+      const int buf = tcount & 1;
+      const uint32_t use = (tcount >> 1) & 1;
+      if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2))) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + buf * 256;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t *sa_p = smem + s * kStageBytes;
+        if constexpr (TR::red) {
+          const int valid = t.rows - kb * BK;
+          if (valid < BK) {
+            // zero K rows [valid, 64) of every box of A and B (128 B each)
+            const int nz = (BK - valid) * (A_BOXES + B_BOXES);
+            for (int i = lane; i < nz * 8; i += 32) {
+              const int line = i >> 3, chunk = i & 7;
+              const int box = line / (BK - valid), r = valid + line % (BK - valid);
+              uint8_t *base = box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192;
+              *reinterpret_cast<uint4 *>(base + r * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t sa = smem_u32(sa_p);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            uint64_t ad, bd;
+            if constexpr (TR::a_mn) ad = smem_desc(sa + ks * 2048, 8192, 1024);
+            else ad = smem_desc(sa + ks * 32, 16, 1024);
+            if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
+            else bd = smem_desc(sb + ks * 32, 16, 1024);
+            tc_mma(dcol, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&st.empty[s]));
+          issued_any = true;
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(smem_u32(&st.tfull[buf]));
+      __syncwarp();
+    }
+    // drain: all issued MMAs complete before TMEM is released
+    if (lane == 0 && issued_any) {
+      tc_commit(smem_u32(&st.drain));
+      const uint32_t bar = smem_u32(&st.drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(bar, 0) && globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue =======================
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    int tcount = 0;
+    for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x, ++tcount) {
+      const Tile t = decode_tile<MODE, BN>(p, st, ti);
+      const int buf = tcount & 1;
+      const uint32_t use = (tcount >> 1) & 1;
+      if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
+      const int r_loc = t.m * BM + q * 32 + lane;
+      if constexpr (TR::red) {
+        float *out = reinterpret_cast<float *>(p.out0) + (int64_t)t.g * p.M_fixed * p.N +
+                     (int64_t)r_loc * p.N + t.n * BN;
+        const bool empty = t.rows <= 0;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          if (empty) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(out + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      } else {
+        const bool valid = r_loc < t.rows;
+        const int64_t row = (int64_t)t.row0 + r_loc;
+        if constexpr (MODE == GU) {
+          __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.F + t.n * 128;
+          __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(p.out1);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float g[32], u[32];
+            tmem_ld32(tbase + c * 32, g);
+            tmem_ld32(tbase + 128 + c * 32, u);
+            if (valid) {
+              float h[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                store16<__nv_bfloat16>(H + c * 32 + i, *reinterpret_cast<float(*)[8]>(h + i));
+              }
+              if (As != nullptr) {
+                __nv_bfloat16 *ag = As + row * 2 * p.F + t.n * 128 + c * 32;
+                __nv_bfloat16 *au = ag + p.F;
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                  store16<__nv_bfloat16>(ag + i, *reinterpret_cast<float(*)[8]>(g + i));
+                  store16<__nv_bfloat16>(au + i, *reinterpret_cast<float(*)[8]>(u + i));
+                }
+              }
+            }
+          }
+        } else if constexpr (MODE == DOWN) {
+          __nv_bfloat16 *Y = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.N + t.n * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8)
+                store16<__nv_bfloat16>(Y + c * 32 + i, *reinterpret_cast<float(*)[8]>(v + i));
+            }
+          }
+        } else if constexpr (MODE == DH) {
+          const __nv_bfloat16 *As = reinterpret_cast<const __nv_bfloat16 *>(p.aux) + row * 2 * p.F + t.n * BN;
+          __nv_bfloat16 *dA = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * 2 * p.F + t.n * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float dh[32];
+            tmem_ld32(tbase + c * 32, dh);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 8) {
+                float G[8], U[8], dG[8], dU[8];
+                load16<__nv_bfloat16>(As + c * 32 + i, G);
+                load16<__nv_bfloat16>(As + p.F + c * 32 + i, U);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float sg = 1.0f / (1.0f + __expf(-G[j]));
+                  dG[j] = dh[i + j] * U[j] * sg * (1.0f + G[j] * (1.0f - sg));
+                  dU[j] = dh[i + j] * G[j] * sg;
+                }
+                store16<__nv_bfloat16>(dA + c * 32 + i, dG);
+                store16<__nv_bfloat16>(dA + p.F + c * 32 + i, dU);
+              }
+            }
+          }
+        } else {  // DX
+          float *o = reinterpret_cast<float *>(p.out0) + row * p.N + t.n * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4 *>(o + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&st.tempty[buf]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void *ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [outer, inner] row-major (inner contiguous), box
+// {64 inner, box_outer}, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedState) + 1024;
+
+template <int MODE, int BN>
+cudaError_t launch_mode(const TcParams &p, cudaStream_t s) {
+  auto k = tc_gemm_kernel<MODE, BN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k<<<num_sms(), kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
+  if (MODE == GU || p.N % 256 != 0) return launch_mode<MODE, 128>(p, s);
+  return launch_mode<MODE, 256>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
+  const int d = a.d, F = a.F, E = a.n_groups;
+  void *H = a.H_save ? a.H_save : a.H_tmp;
+  TcParams p{};
+  p.n_groups = E; p.max_rows = a.max_rows; p.d = d; p.F = F; p.offsets = a.offsets;
+  p.status = a.status;
+  // GU
+  if (!make_map(&p.tmA, a.Xp, d, a.max_rows, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&p.tmB, a.W_gu, d, (uint64_t)E * 2 * F, 128)) return cudaErrorInvalidValue;
+  p.mode = GU; p.N = F; p.K_fixed = d; p.b_group_rows = 2 * (int64_t)F;
+  p.out0 = H; p.out1 = a.A_save;
+  cudaError_t e = launch_bn<GU>(p, s);
+  if (e != cudaSuccess) return e;
+  // DOWN
+  TcParams q = p;
+  if (!make_map(&q.tmA, H, F, a.max_rows, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, 128)) return cudaErrorInvalidValue;
+  q.mode = DOWN; q.N = d; q.K_fixed = F; q.b_group_rows = d; q.out0 = a.Yp; q.out1 = nullptr;
+  return launch_bn<DOWN>(q, s);
+}
+
+cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
+  const int d = a.d, F = a.F, E = a.n_groups;
+  TcParams p{};
+  p.n_groups = E; p.max_rows = a.max_rows; p.d = d; p.F = F; p.offsets = a.offsets;
+  p.status = a.status;
+  cudaError_t e;
+  {  // DH: dA = swiglu'(dYp W_down)
+    TcParams q = p;
+    if (!make_map(&q.tmA, a.dYp, d, a.max_rows, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, 64)) return cudaErrorInvalidValue;
+    q.mode = DH; q.N = F; q.K_fixed = d; q.b_group_rows = d; q.out0 = a.dA; q.aux = a.A_save;
+    if ((e = launch_bn<DH>(q, s)) != cudaSuccess) return e;
+  }
+  {  // DX: dXp = dA W_gu
+    TcParams q = p;
+    if (!make_map(&q.tmA, a.dA, 2 * F, a.max_rows, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.W_gu, d, (uint64_t)E * 2 * F, 64)) return cudaErrorInvalidValue;
+    q.mode = DX; q.N = d; q.K_fixed = 2 * F; q.b_group_rows = 2 * (int64_t)F; q.out0 = a.dXp;
+    if ((e = launch_bn<DX>(q, s)) != cudaSuccess) return e;
+  }
+  {  // WGD: dW_down[g] = dYp_g^T H_g
+    TcParams q = p;
+    if (!make_map(&q.tmA, a.dYp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.H_save, F, a.max_rows, 64)) return cudaErrorInvalidValue;
+    q.mode = WGD; q.M_fixed = d; q.N = F; q.out0 = a.dW_down;
+    if ((e = launch_bn<WGD>(q, s)) != cudaSuccess) return e;
+  }
+  {  // WGU: dW_gu[g] = dA_g^T Xp_g
+    TcParams q = p;
+    if (!make_map(&q.tmA, a.dA, 2 * F, a.max_rows, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.Xp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
+    q.mode = WGU; q.M_fixed = 2 * F; q.N = d; q.out0 = a.dW_gu;
+    if ((e = launch_bn<WGU>(q, s)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe

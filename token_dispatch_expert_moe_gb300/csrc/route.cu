@@ -1,0 +1,219 @@
+// Router: logits GEMV, softmax, Top-K, combine weights; capacity dropping.
+//
+// MoE Parallel Folding (arXiv 2504.14960) study notes: "method overview" (the
+// router assigns each token its Top-K experts), "prerequisites" (Top-K gating,
+// capacity factor), "key modules" and the quoted section 3.3 (drops are
+// decided inside each sub-sequence; sub-sequence dropping is the default).
+//
+// The softmax and Top-K arithmetic is specified in softmax.cuh.
+#include "common.cuh"
+#include "softmax.cuh"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Fused router: one warp per token; the CTA stages a chunk of W_r (and w_sg)
+// in shared memory as fp32 and every warp reuses it for its token.
+constexpr int kRouteWarps = 8;
+constexpr int kRouteChunk = 256;  // hidden elements per stage
+
+template <typename T>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+router_fused_kernel(RouteArgs a) {
+  extern __shared__ float wsm[];  // [C][kRouteChunk], C = E (+1 for w_sg)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = a.E;
+  const int C = E + (a.w_sg != nullptr ? 1 : 0);
+  const int64_t t = (int64_t)blockIdx.x * kRouteWarps + warp;
+  const bool active = t < a.T;
+  const T *x = reinterpret_cast<const T *>(a.x);
+  const T *W = reinterpret_cast<const T *>(a.W_r);
+  const T *wsg = reinterpret_cast<const T *>(a.w_sg);
+
+  float acc[65];
+#pragma unroll
+  for (int c = 0; c < 65; ++c) acc[c] = 0.0f;
+
+  for (int j0 = 0; j0 < a.d; j0 += kRouteChunk) {
+    const int n = min(kRouteChunk, a.d - j0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < C * kRouteChunk; i += blockDim.x) {
+      const int c = i / kRouteChunk, j = i % kRouteChunk;
+      float v = 0.0f;
+      if (j < n) v = to_f32(c < E ? W[(int64_t)c * a.d + j0 + j] : wsg[j0 + j]);
+      wsm[i] = v;
+    }
+    __syncthreads();
+    if (active) {
+      // lane owns hidden elements j = lane + 32*i of this chunk
+      float xv[kRouteChunk / 32];
+#pragma unroll
+      for (int i = 0; i < kRouteChunk / 32; ++i) {
+        const int j = lane + 32 * i;
+        xv[i] = j < n ? to_f32(x[t * a.d + j0 + j]) : 0.0f;
+      }
+#pragma unroll
+      for (int c = 0; c < 65; ++c) {
+        if (c < C) {
+          float part = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kRouteChunk / 32; ++i)
+            part = fmaf(xv[i], wsm[c * kRouteChunk + lane + 32 * i], part);
+          acc[c] += part;
+        }
+      }
+    }
+  }
+  if (!active) return;
+  // fixed-order butterfly reduction of each column over the lanes
+#pragma unroll
+  for (int c = 0; c < 65; ++c) {
+    if (c < C) acc[c] = warp_sum(acc[c]);
+  }
+  float l0 = 0.0f, l1 = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    if (c == lane) l0 = acc[c];
+    if (c == lane + 32) l1 = acc[c];
+  }
+  if (a.b_r != nullptr) {
+    if (lane < E) l0 = __fadd_rn(l0, a.b_r[lane]);
+    if (lane + 32 < E) l1 = __fadd_rn(l1, a.b_r[lane + 32]);
+  }
+  if (lane < E) a.logits[t * E + lane] = l0;
+  if (lane + 32 < E) a.logits[t * E + lane + 32] = l1;
+  if (a.w_sg != nullptr && lane == 0) {
+    float z = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 65; ++c)
+      if (c == E) z = acc[c];
+    a.gate_logit[t] = z;
+  }
+  spec::softmax_topk_warp(l0, l1, E, a.K, a.renorm, a.topk_idx + t * a.K, a.topk_prob + t * a.K,
+                    a.topk_w + t * a.K, a.keep + t * a.K);
+}
+
+__global__ void __launch_bounds__(256) topk_from_logits_kernel(RouteArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= a.T) return;
+  const float *l = a.logits + t * a.E;
+  const float l0 = lane < a.E ? l[lane] : 0.0f;
+  const float l1 = lane + 32 < a.E ? l[lane + 32] : 0.0f;
+  spec::softmax_topk_warp(l0, l1, a.E, a.K, a.renorm, a.topk_idx + t * a.K, a.topk_prob + t * a.K,
+                    a.topk_w + t * a.K, a.keep + t * a.K);
+}
+
+// ---------------------------------------------------------------------------
+// Capacity dropping: one CTA per (sub-sequence j, expert e). Candidates are
+// the assignments (t, k) of the sub-sequence routed to e, keyed by
+// (fp32 bits of p) << 32 | (2^32 - 1 - t): a larger key is a higher
+// probability, then a lower token index. Keys are unique, so the cap largest
+// are found exactly by an 8-pass MSB radix select of the cap-th largest key.
+constexpr int kCapThreads = 512;
+
+__global__ void __launch_bounds__(kCapThreads)
+capacity_kernel(RouteArgs a, int cap_full, int cap_last) {
+  __shared__ uint32_t n_cand;
+  __shared__ uint32_t hist[256];
+  __shared__ unsigned long long sh_prefix;
+  __shared__ uint32_t sh_need;
+  const int j = blockIdx.x, e = blockIdx.y;
+  const int64_t lo = (int64_t)j * a.S;
+  const int64_t hi = min(a.T, lo + a.S);
+  const int cap = (hi - lo == a.S) ? cap_full : cap_last;
+  unsigned long long *keys = a.cap_keys + ((int64_t)j * a.E + e) * a.S;
+  const int K = a.K;
+  if (threadIdx.x == 0) n_cand = 0;
+  __syncthreads();
+  for (int64_t t = lo + threadIdx.x; t < hi; t += blockDim.x) {
+    for (int k = 0; k < K; ++k) {
+      if (a.topk_idx[t * K + k] == e) {
+        const uint32_t pos = atomicAdd(&n_cand, 1u);
+        const uint32_t pbits = __float_as_uint(a.topk_prob[t * K + k]);
+        keys[pos] = ((unsigned long long)pbits << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t n = n_cand;
+  unsigned long long threshold = 0;
+  if (n > (uint32_t)cap) {
+    if (threadIdx.x == 0) { sh_prefix = 0; sh_need = (uint32_t)cap; }
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
+      __syncthreads();
+      const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+      const unsigned long long pre = sh_prefix;
+      for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+        const unsigned long long key = keys[i];
+        if ((key & hmask) == (pre & hmask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint32_t need = sh_need, cum = 0;
+        int digit = 0;
+        for (int b = 255; b >= 0; --b) {
+          if (cum + hist[b] >= need) { digit = b; need -= cum; break; }
+          cum += hist[b];
+        }
+        sh_need = need;
+        sh_prefix = pre | ((unsigned long long)digit << shift);
+      }
+      __syncthreads();
+    }
+    threshold = sh_prefix;
+  }
+  for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const unsigned long long key = keys[i];
+    const int64_t t = (int64_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+    for (int k = 0; k < K; ++k) {
+      if (a.topk_idx[t * K + k] == e) a.keep[t * K + k] = key >= threshold ? 1 : 0;
+    }
+  }
+}
+
+int capacity_of(float cf, int64_t S_j, int K, int E) {
+  // ceil(CF * S_j * K / E) in double, left to right
+  double v = (double)cf * (double)S_j * (double)K / (double)E;
+  return (int)ceil(v);
+}
+
+}  // namespace
+
+cudaError_t launch_router_fused(const RouteArgs &a, cudaStream_t s) {
+  const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
+  const size_t smem = (size_t)C * kRouteChunk * sizeof(float);
+  const unsigned grid = (unsigned)((a.T + kRouteWarps - 1) / kRouteWarps);
+  if (a.dtype == MOE_BF16) {
+    auto k = router_fused_kernel<__nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kRouteWarps * 32, smem, s>>>(a);
+  } else {
+    auto k = router_fused_kernel<float>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kRouteWarps * 32, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_from_logits(const RouteArgs &a, cudaStream_t s) {
+  const unsigned grid = (unsigned)((a.T * 32 + 255) / 256);
+  topk_from_logits_kernel<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s) {
+  const int64_t n_sub = (a.T + a.S - 1) / a.S;
+  const int64_t last = a.T - (n_sub - 1) * a.S;
+  const int cap_full = capacity_of(a.cf, a.S, a.K, a.E);
+  const int cap_last = capacity_of(a.cf, last, a.K, a.E);
+  dim3 grid((unsigned)n_sub, (unsigned)a.E);
+  capacity_kernel<<<grid, kCapThreads, 0, s>>>(a, cap_full, cap_last);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

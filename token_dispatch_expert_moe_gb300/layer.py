@@ -1,0 +1,126 @@
+"""MoELayer: the whole layer through the C ABI, buffers held in torch tensors.
+
+Forward: moe_route -> moe_permute -> moe_expert_ffn (routed experts)
+[-> moe_expert_ffn (shared expert: one group, offsets {0, T})] -> moe_unpermute.
+Backward: moe_unpermute_bwd -> moe_expert_ffn_bwd (routed [, shared]) ->
+moe_route_bwd -> moe_permute_bwd.
+torch only allocates device memory and supplies the stream; every step runs
+in libmoe.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _lib as L
+
+
+def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """Host array -> device tensor; uint16 arrays are bf16 bit patterns."""
+    if a.dtype == np.uint16:
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+class MoELayer:
+    """One MoE layer of configuration `cfg` (a synthetic.MoEConfig-like object)
+    with device weights W_r, W_gu, W_down (+ b_r, w_sg, Ws_gu, Ws_down)."""
+
+    def __init__(self, cfg, weights: dict, device="cuda", backward=None):
+        self.cfg = cfg
+        self.shape = L.shape_of(cfg)
+        self.backward_enabled = cfg.backward if backward is None else backward
+        self.w = weights
+        T, d, E, K, F = cfg.T, cfg.d, cfg.E, cfg.K, cfg.F
+        dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        self.dt = dt
+        self.dtype_code = L.MOE_BF16 if cfg.dtype == "bf16" else L.MOE_F32
+        N = T * K
+        z = lambda *s, dtype=dt: torch.empty(*s, dtype=dtype, device=device)  # noqa: E731
+        self.ws = torch.zeros(L.moe_workspace_size(self.shape), dtype=torch.uint8, device=device)
+        self.logits = z(T, E, dtype=torch.float32)
+        self.topk_idx = z(T, K, dtype=torch.int32)
+        self.topk_prob = z(T, K, dtype=torch.float32)
+        self.topk_w = z(T, K, dtype=torch.float32)
+        self.keep = z(T, K, dtype=torch.uint8)
+        self.Xp = z(N, d)
+        self.row_of = z(T, K, dtype=torch.int32)
+        self.src_of = z(N, dtype=torch.int32)
+        self.counts = z(E, dtype=torch.int32)
+        self.offsets = z(E + 1, dtype=torch.int32)
+        self.A_save = z(N, 2 * F) if self.backward_enabled else None
+        self.H = z(N, F)
+        self.Yp = z(N, d)
+        self.out = z(T, d)
+        self.shared = cfg.Fs > 0
+        if self.shared:
+            Fs = cfg.Fs
+            self.gate_logit = z(T, dtype=torch.float32)
+            self.off1 = torch.tensor([0, T], dtype=torch.int32, device=device)
+            self.As = z(T, 2 * Fs) if self.backward_enabled else None
+            self.Hs = z(T, Fs)
+            self.Ys = z(T, d)
+        else:
+            self.gate_logit = self.Ys = None
+        if self.backward_enabled:
+            self.dYp = z(N, d)
+            self.dw = z(T, K, dtype=torch.float32)
+            self.dA = z(N, 2 * F)
+            self.dXp = z(N, d, dtype=torch.float32)
+            self.dW_gu = z(E, 2 * F, d, dtype=torch.float32)
+            self.dW_down = z(E, d, F, dtype=torch.float32)
+            self.dW_r = z(E, d, dtype=torch.float32)
+            self.db_r = z(E, dtype=torch.float32)
+            self.dx_router = z(T, d, dtype=torch.float32)
+            self.dx = z(T, d, dtype=torch.float32)
+            if self.shared:
+                Fs = cfg.Fs
+                self.dYs = z(T, d)
+                self.dz = z(T, dtype=torch.float32)
+                self.dAs = z(T, 2 * Fs)
+                self.dXs = z(T, d, dtype=torch.float32)
+                self.dWs_gu = z(2 * Fs, d, dtype=torch.float32)
+                self.dWs_down = z(d, Fs, dtype=torch.float32)
+                self.dw_sg = z(d, dtype=torch.float32)
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        c, s, w = self.cfg, self.shape, self.w
+        self.x = x
+        L.moe_route(s, x, w["W_r"], w.get("b_r"), w.get("w_sg"), self.logits, self.gate_logit,
+                    self.topk_idx, self.topk_prob, self.topk_w, self.keep, self.ws, stream)
+        L.moe_permute(s, x, self.topk_idx, self.keep, self.Xp, self.row_of, self.src_of,
+                      self.counts, self.offsets, self.ws, stream)
+        L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.Xp,
+                         w["W_gu"], w["W_down"], self.A_save, self.H, self.Yp, self.ws, stream)
+        if self.shared:
+            L.moe_expert_ffn(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, x, w["Ws_gu"],
+                             w["Ws_down"], self.As, self.Hs, self.Ys, self.ws, stream)
+        L.moe_unpermute(s, self.Yp, self.row_of, self.topk_w, self.Ys, self.gate_logit, self.out,
+                        stream)
+        return self.out
+
+    def backward(self, dout: torch.Tensor, stream=None) -> dict:
+        c, s, w = self.cfg, self.shape, self.w
+        L.moe_unpermute_bwd(s, dout, self.Yp, self.row_of, self.topk_w, self.Ys, self.gate_logit,
+                            self.dYp, self.dw, self.dYs if self.shared else None,
+                            self.dz if self.shared else None, stream)
+        L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.dYp,
+                             self.Xp, self.A_save, self.H, w["W_gu"], w["W_down"], self.dA,
+                             self.dXp, self.dW_gu, self.dW_down, self.ws, stream)
+        dx_in = None
+        if self.shared:
+            L.moe_expert_ffn_bwd(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, self.dYs, self.x,
+                                 self.As, self.Hs, w["Ws_gu"], w["Ws_down"], self.dAs, self.dXs,
+                                 self.dWs_gu, self.dWs_down, self.ws, stream)
+            dx_in = self.dXs
+        L.moe_route_bwd(s, self.x, w["W_r"], w.get("w_sg"), self.logits, self.topk_idx,
+                        self.topk_prob, self.topk_w, self.dw, self.dz if self.shared else None,
+                        dx_in, self.dW_r, self.db_r if "b_r" in w else None,
+                        self.dw_sg if self.shared else None, self.dx_router, self.ws, stream)
+        L.moe_permute_bwd(s, self.dXp, self.row_of, self.dx_router, self.dx, stream)
+        g = {"dx": self.dx, "dW_r": self.dW_r, "dW_gu": self.dW_gu, "dW_down": self.dW_down}
+        if "b_r" in w:
+            g["db_r"] = self.db_r
+        if self.shared:
+            g.update(dWs_gu=self.dWs_gu, dWs_down=self.dWs_down, dw_sg=self.dw_sg)
+        return g
