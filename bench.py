@@ -1,0 +1,386 @@
+"""Benchmark of the single-GPU MoE layer (tokens/s) on synthetic inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+A step is one pass of the layer's hot path over one batch: route (logits,
+softmax, Top-K, capacity), permute, grouped SwiGLU FFN, un-permute (+ the
+backward chain for workloads that train). The default workload is the
+Mixtral-8x22B-shaped layer: T=8192 tokens (2 x 4096), d=6144, E=8, Top-2,
+SwiGLU ffn 16384, capacity factor 1 per 4096-token sub-sequence, forward.
+
+Timing: W untimed warm-up steps, then K steps in one region bracketed by a
+barrier and cudaDeviceSynchronize, timed with CUDA events on the launching
+stream; the max over ranks is reported. Each step streams every expert weight
+(4.9 GB for the default workload) through the 129 MB L2, so no step starts
+with its inputs in L2. SM clocks and throttle reasons are sampled with
+nvidia-smi during the timed region.
+
+`e2e` repeats the measurement through the C ABI with host buffers: each step
+copies the tokens from pinned host memory to the device and the layer output
+back, inside the timed region.
+
+`--impl reference` times the CPU oracle (the plain numpy definition of the
+layer) on the host cores instead, on a bounded sample of the same workload.
+
+With N > 1 (under torchrun) every rank runs an independent replica on its
+own batch (weak scaling); `value` is the tokens of all ranks / the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "mixtral_8x22b"
+METRIC = "MoE layer tokens/s on 1 GB300"
+
+
+# ---------------------------------------------------------------------------
+# multi-rank bookkeeping (host logic; also exercised by CPU tests with gloo)
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(tokens_per_rank: float, seconds_per_rank: float, world: int, dist=None) -> dict:
+    """Whole-job throughput: all ranks' tokens / the slowest rank's time."""
+    secs = seconds_per_rank
+    toks = tokens_per_rank
+    if world > 1 and dist is not None:
+        import torch
+        t = torch.tensor([secs], dtype=torch.float64)
+        n = torch.tensor([toks], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            t, n = t.cuda(), n.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        secs, toks = float(t.item()), float(n.item())
+    else:
+        toks = toks * world
+    return {"seconds": secs, "tokens": toks, "value": toks / secs}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + SMI_FIELDS,
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+
+def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = None) -> dict:
+    """Time the oracle as it stands on a bounded sample and scale to tokens/s.
+
+    Routing, map, permute and combine run on `token_cap` tokens (all T by
+    default); the expert FFN runs the oracle's per-expert group routine on
+    `ffn_rows` rows of expert 0 (weight decode + the rows' GEMMs), scaled to
+    every expert's decode and all kept rows."""
+    from oracle import moe_oracle as O
+    T = cfg.T if token_cap is None else min(cfg.T, token_cap)
+    sub = dict(inp)
+    sub["x"] = inp["x"][:T]
+    import dataclasses
+    c = dataclasses.replace(cfg, T=T)
+    t0 = time.perf_counter()
+    r = O.route(c, sub)
+    counts, offsets, row_of, src_of, n_kept = O.build_map(r["topk_idx"], r["keep"], c.E)
+    Xp = O.permute(sub["x"], src_of, c.K)
+    t_route = time.perf_counter() - t0
+    rows = np.arange(min(ffn_rows, max(1, int(counts[0]))))
+    t1 = time.perf_counter()
+    Wgu = O.decode(inp["W_gu"][0])
+    Wd = O.decode(inp["W_down"][0])
+    t_decode = time.perf_counter() - t1
+    t2 = time.perf_counter()
+    O.swiglu_group(O.decode(Xp[rows + offsets[0]]), Wgu, Wd, O.act_rounder(cfg.dtype, True))
+    t_rows = time.perf_counter() - t2
+    Yp = np.zeros((n_kept, c.d))
+    t3 = time.perf_counter()
+    O.unpermute(Yp, row_of, r["topk_w"], dtype=c.dtype)
+    t_comb = time.perf_counter() - t3
+    n_full = n_kept * cfg.T / T
+    total = (t_route + t_comb) * cfg.T / T + cfg.E * t_decode + t_rows * n_full / len(rows)
+    if cfg.Fs:
+        total += t_rows * cfg.T / len(rows) * cfg.Fs / cfg.F
+    if cfg.backward:
+        total *= 3.0   # backward: two GEMMs per forward GEMM (dgrad + wgrad)
+    wall = time.perf_counter() - t0
+    return {"value": cfg.T / total, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": (f"routing, map, permute and combine on {T} of {cfg.T} tokens; expert FFN "
+                       f"on {len(rows)} rows of expert 0 plus one expert's weight decode, "
+                       f"scaled to {cfg.E} experts and {int(n_full)} kept rows"
+                       + ("; backward counted as 2x the forward GEMMs" if cfg.backward else "")),
+            "sample_seconds": round(wall, 2)}
+
+
+# ---------------------------------------------------------------------------
+
+def launches_per_step(cfg) -> int:
+    n = 1 + (1 if cfg.drop else 0)        # router (+ capacity)
+    n += 4                                 # map count, scan, scatter, row copy
+    n += 2 + (2 if cfg.Fs else 0)          # grouped GEMMs (routed [+ shared])
+    n += 1                                 # un-permute
+    if cfg.backward:
+        n += 1                             # un-permute backward
+        n += 4 + (4 if cfg.Fs else 0)      # dH, dX, dW_down, dW_gu GEMMs
+        n += 4 + (1 if cfg.bias else 0)    # router backward
+        n += 1                             # permute backward
+    return n
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return
+    from synthetic import make_inputs
+    inp = make_inputs(cfg, need_backward=False)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = oracle_throughput(cfg, inp, ffn_rows=64, token_cap=1024)
+        if i >= args.warmup:
+            vals.append(r["value"])
+    v = statistics.median(vals)
+    cpu = dict(r, value=v)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * cfg.T / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(cfg), "cpu_baseline": cpu,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg) -> dict:
+    return {"workload": (f"{cfg.name} MoE layer {'fwd+bwd' if cfg.backward else 'fwd'}: T={cfg.T}, "
+                         f"d={cfg.d}, E={cfg.E}, top-{cfg.K}, SwiGLU ffn={cfg.F}"
+                         + (f", shared ffn={cfg.Fs}" if cfg.Fs else "")
+                         + (f", capacity factor {cfg.cf} per {cfg.subseq}-token sub-sequence"
+                            if cfg.drop else ", dropless")),
+            "tokens_per_step": cfg.T, "l2": "inputs larger than L2 (all expert weights stream every step)",
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    from synthetic import get_config, make_inputs
+    cfg = get_config(args.config)
+    rank, world, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl != "reference" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, cfg, rank, world)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    from token_dispatch_expert_moe_gb300 import _lib as L
+    from token_dispatch_expert_moe_gb300.layer import MoELayer, to_device
+    import dataclasses
+    cfg_r = dataclasses.replace(cfg, seed=cfg.seed + rank)   # each replica its own batch
+    inp = make_inputs(cfg_r)
+    w = {k: to_device(v) for k, v in inp.items() if k not in ("x", "dout")}
+    layer = MoELayer(cfg_r, w)
+    x = to_device(inp["x"])
+    dout = to_device(inp["dout"]) if cfg.backward else None
+    stream = torch.cuda.current_stream()
+
+    ffn_ev, perm_ev, unperm_ev = [], [], []
+
+    def step(record=False):
+        c, s, ws = cfg_r, layer.shape, layer.ws
+        L.moe_route(s, x, w["W_r"], w.get("b_r"), w.get("w_sg"), layer.logits, layer.gate_logit,
+                    layer.topk_idx, layer.topk_prob, layer.topk_w, layer.keep, ws)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+        if record: e[0].record(stream)
+        L.moe_permute(s, x, layer.topk_idx, layer.keep, layer.Xp, layer.row_of, layer.src_of,
+                      layer.counts, layer.offsets, ws)
+        if record: e[1].record(stream)
+        if record: e[2].record(stream)
+        L.moe_expert_ffn(layer.dtype_code, c.T * c.K, c.d, c.F, c.E, layer.offsets, layer.Xp,
+                         w["W_gu"], w["W_down"], layer.A_save, layer.H, layer.Yp, ws)
+        if record: e[3].record(stream)
+        if c.Fs:
+            L.moe_expert_ffn(layer.dtype_code, c.T, c.d, c.Fs, 1, layer.off1, x, w["Ws_gu"],
+                             w["Ws_down"], layer.As, layer.Hs, layer.Ys, ws)
+        if record: e[4].record(stream)
+        L.moe_unpermute(s, layer.Yp, layer.row_of, layer.topk_w, layer.Ys, layer.gate_logit,
+                        layer.out)
+        if record: e[5].record(stream)
+        if c.backward:
+            layer.backward(dout)
+        if record:
+            perm_ev.append((e[0], e[1]))
+            ffn_ev.append((e[2], e[3]))
+            unperm_ev.append((e[4], e[5]))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc, info = L.moe_get_status(layer.ws)
+    assert rc == 0, f"device status {rc} info {info:#x}"
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    time.sleep(0.4)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    secs = t_start.elapsed_time(t_end) / 1e3
+    agg = aggregate(cfg.T * args.steps, secs, world, dist)
+
+    n_kept = int(layer.offsets[-1].item())
+    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
+    perm_ms = statistics.mean(a.elapsed_time(b) for a, b in perm_ev)
+    unperm_ms = statistics.mean(a.elapsed_time(b) for a, b in unperm_ev)
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured (burst)" if "bf16_tflops" in peaks else "fallback"
+    flops = 6.0 * n_kept * cfg.d * cfg.F
+    achieved = flops / (ffn_ms * 1e-3) / 1e12
+    b = 2 if cfg.dtype == "bf16" else 4
+    perm_bytes = cfg.T * cfg.d * b + n_kept * cfg.d * b + cfg.T * cfg.K * 9
+    unperm_bytes = n_kept * cfg.d * b + cfg.T * cfg.d * b + cfg.T * cfg.K * 8
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        import hashlib
+        ent = json.load(open(tr_path)).get(f"{cfg.name}:grouped_gemm")
+        src = os.path.join(ROOT, "token_dispatch_expert_moe_gb300", "csrc", "gemm_tc.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent is not None and ent.get("source_sha") == sha:   # counters of this very kernel
+            traffic = ent["bytes"]
+
+    # e2e through the C ABI with host buffers
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    out_host = torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
+    for _ in range(2):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(layer.out, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(layer.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = aggregate(cfg.T * args.steps, e0.elapsed_time(e1) / 1e3, world, dist)
+    h2d = x.numel() * x.element_size()
+    d2h = layer.out.numel() * layer.out.element_size()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": agg["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * agg["seconds"] / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic (seeded normal inputs, random-init weights)",
+            "config": workload_config(cfg),
+            "clocks": clk,
+            "e2e": {"value": e2e["value"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step(cfg) * args.steps,
+            "roofline": {"kernel": "grouped SwiGLU GEMM (moe_expert_ffn: gate/up + down)",
+                         "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,
+                         "peak_source": peak_src,
+                         "flops_per_launch": flops, "ms_per_launch": ffn_ms},
+            "stages": {
+                "n_kept": n_kept,
+                "permute_ms": perm_ms, "permute_GBps": perm_bytes / perm_ms / 1e6,
+                "permute_hbm_frac": perm_bytes / perm_ms / 1e6 / hbm_peak,
+                "unpermute_ms": unperm_ms, "unpermute_GBps": unperm_bytes / unperm_ms / 1e6,
+                "unpermute_hbm_frac": unperm_bytes / unperm_ms / 1e6 / hbm_peak,
+                "hbm_peak_GBps": hbm_peak,
+            },
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_throughput(cfg, inp)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

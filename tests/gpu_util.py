@@ -26,6 +26,19 @@ SMALL = ["tiny_f32", "mixtral_8x22b@small", "qwen2_57b_a14b@small",
 FULL = ["mixtral_8x22b", "qwen2_57b_a14b", "mixtral_8x22b_g8t8", "llama3_8x70b"]
 
 
+_INPUT_CACHE = {}
+
+
+def inputs(cfg, need_backward=None):
+    """make_inputs with a one-entry cache (full-size weights take seconds)."""
+    key = (cfg, need_backward)
+    if key not in _INPUT_CACHE:
+        _INPUT_CACHE.clear()
+        from synthetic import make_inputs
+        _INPUT_CACHE[key] = make_inputs(cfg, need_backward=need_backward)
+    return _INPUT_CACHE[key]
+
+
 def lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")

@@ -1,0 +1,57 @@
+"""bench.py host logic without a GPU: whole-job aggregation over ranks
+(tokens summed, slowest rank's time) with two gloo ranks, and the launch
+count per step."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    r = bench.aggregate(tokens_per_rank=1000.0 * (rank + 1), seconds_per_rank=0.5 + rank,
+                        world=world, dist=dist)
+    q.put((rank, r))
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in res.values():
+        assert r["tokens"] == 3000.0 and r["seconds"] == 1.5
+        assert abs(r["value"] - 2000.0) < 1e-9
+
+
+def test_aggregate_single_rank():
+    import bench
+    r = bench.aggregate(8192.0, 2.0, 1)
+    assert r["value"] == 4096.0
+
+
+def test_launch_counts():
+    import bench
+    from synthetic import get_config
+    assert bench.launches_per_step(get_config("mixtral_8x22b")) == 9
+    assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 10
+    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 15

@@ -9,7 +9,7 @@ import pytest
 
 from oracle import moe_oracle as O
 from synthetic import get_config, make_inputs
-from tests.gpu_util import FULL, SMALL, act_dtype, assert_close, bf16_bits, dev, empty, host, lib, torch
+from tests.gpu_util import inputs, FULL, SMALL, act_dtype, assert_close, bf16_bits, dev, empty, host, lib, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +47,7 @@ def _check_permute(L, cfg, x, idx, keep):
 def test_permute(name):
     L = lib()
     cfg = get_config(name)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     r = O.route(cfg, inp)
     _check_permute(L, cfg, inp["x"], r["topk_idx"], r["keep"])
 
@@ -62,7 +62,7 @@ def test_permute_edge_cases(case):
         cfg = dataclasses.replace(base, T=1)
     if case == "ragged_T":
         cfg = dataclasses.replace(base, T=257)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     T, K, E = cfg.T, cfg.K, cfg.E
     idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
     keep = (rng.random((T, K)) < 0.8).astype(np.uint8)
@@ -99,7 +99,7 @@ def _as_act(cfg, v):
 def test_unpermute(name):
     L = lib()
     cfg = get_config(name)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     f = O.layer_forward(cfg, inp)
     Ys = _as_act(cfg, f["Ys"]) if cfg.Fs else None
     z = f["gate_logit"].astype(np.float32) if cfg.Fs else None
@@ -128,7 +128,7 @@ def test_identity_experts_round_trip():
     K x exactly in bf16 (dropless)."""
     L = lib()
     cfg = dataclasses.replace(get_config("qwen2_57b_a14b@small"), T=640, Fs=0)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     r = O.route(cfg, inp)
     o, n = _check_permute(L, cfg, inp["x"], r["topk_idx"], r["keep"])
     got = _unpermute_gpu(L, cfg, o["Xp"], host(o["row_of"]), np.ones((cfg.T, cfg.K), np.float32))

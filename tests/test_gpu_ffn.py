@@ -8,7 +8,7 @@ import pytest
 from oracle import moe_oracle as O
 from synthetic import get_config, make_inputs
 from synthetic.gen import normal_bf16, normal_f32
-from tests.gpu_util import FULL, SMALL, act_dtype, assert_close, dev, empty, host, lib, torch
+from tests.gpu_util import inputs, FULL, SMALL, act_dtype, assert_close, dev, empty, host, lib, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def _check_fwd(L, dtype, Xp_host, offsets, W_gu, W_down, d, F, rows=None):
 def test_ffn_forward(name):
     L = lib()
     cfg = get_config(name)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     r = O.route(cfg, inp)
     _, offsets, _, src_of, n = O.build_map(r["topk_idx"], r["keep"], cfg.E)
     Xp = O.permute(inp["x"], src_of, cfg.K)
@@ -73,7 +73,7 @@ def test_ffn_forward_full_size_sampled(name):
     expert (first, middle, last) checked against the oracle row by row."""
     L = lib()
     cfg = get_config(name)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     r = O.route(cfg, inp)
     _, offsets, _, src_of, n = O.build_map(r["topk_idx"], r["keep"], cfg.E)
     Xp = O.permute(inp["x"], src_of, cfg.K)

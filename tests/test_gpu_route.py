@@ -9,7 +9,7 @@ import pytest
 from oracle import moe_oracle as O
 from synthetic import get_config, make_inputs
 from synthetic.gen import TID, normal_f32
-from tests.gpu_util import FULL, SMALL, bf16_bits, dev, empty, host, lib, rel_frob, torch
+from tests.gpu_util import inputs, FULL, SMALL, bf16_bits, dev, empty, host, lib, rel_frob, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -85,7 +85,7 @@ def test_exp_and_softmax_bits_over_a_wide_range():
 def test_route_fused(name):
     L = lib()
     cfg = get_config(name)
-    inp = make_inputs(cfg, need_backward=False)
+    inp = inputs(cfg, need_backward=False)
     T, E, K = cfg.T, cfg.E, cfg.K
     s = L.shape_of(cfg)
     ws = torch.zeros(L.moe_workspace_size(s), dtype=torch.uint8, device="cuda")
