@@ -137,6 +137,34 @@ moe_status_t moe_permute(const moe_shape_t *shape, const void *x,
                          int32_t *row_of, int32_t *src_of, int32_t *counts,
                          int32_t *offsets, void *ws, moe_stream_t stream);
 
+/* Largest token count T that moe_permute_noalloc accepts. */
+#define MOE_PERMUTE_NOALLOC_MAX_TOKENS 131072
+
+/* moe_permute for callers that cannot allocate device memory: the same
+ * outputs as moe_permute (bit for bit), with no workspace argument. The paper
+ * has no counterpart; this is a convenience of this library.
+ * Who needs it: code that runs where cudaMalloc is not allowed or not safe --
+ * inside a custom allocator's callbacks, under a fixed device-memory budget
+ * reserved at start-up (serving processes that pin all memory up front), or
+ * on a latency path that must not risk the implicit device synchronisation a
+ * cudaMalloc/cudaFree can cause.
+ * How: the map build's scratch (per-block expert counts, 128 KB) is a fixed
+ * array inside libmoe.so, resident on every GPU that loads the library until
+ * the process exits. The first call on each device looks the array's device
+ * address up (cudaGetSymbolAddress, with that device current) and caches it;
+ * make that first call before any stream capture. No call allocates.
+ * Limits: T <= MOE_PERMUTE_NOALLOC_MAX_TOKENS, else MOE_ERR_UNSUPPORTED; E <= 64
+ * as everywhere. Every call uses the same array: two calls that can run at the
+ * same time on one GPU (different streams or host threads without ordering
+ * between them) race and corrupt each other's maps; order them. Each call
+ * rewrites all the scratch it reads, so the previous call's contents never
+ * leak into a result. There is no workspace, so no device status word is
+ * recorded: an out-of-range expert index is skipped (its row_of is -1).     */
+moe_status_t moe_permute_noalloc(const moe_shape_t *shape, const void *x,
+                                 const int32_t *topk_idx, const uint8_t *keep, void *Xp,
+                                 int32_t *row_of, int32_t *src_of, int32_t *counts,
+                                 int32_t *offsets, moe_stream_t stream);
+
 /* Grouped SwiGLU FFN (study notes, "method overview": expert FFN
  * computation). Group g owns rows [offsets[g], offsets[g+1]) of Xp.
  *   dtype: MOE_BF16 (tcgen05 tensor-core path) or MOE_F32;

@@ -53,6 +53,7 @@ _SIGS = {
     "moe_route": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_route_topk": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_permute_noalloc": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_expert_ffn": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -132,6 +133,13 @@ def moe_route_topk(shape, logits, topk_idx, topk_prob, topk_w, keep, ws, stream=
 def moe_permute(shape, x, topk_idx, keep, Xp, row_of, src_of, counts, offsets, ws, stream=None):
     _call("moe_permute", ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(keep), _ptr(Xp),
           _ptr(row_of), _ptr(src_of), _ptr(counts), _ptr(offsets), _ptr(ws), _stream(stream))
+
+
+def moe_permute_noalloc(shape, x, topk_idx, keep, Xp, row_of, src_of, counts, offsets,
+                        stream=None):
+    """moe_permute without a workspace (scratch inside libmoe.so); see moe.h."""
+    _call("moe_permute_noalloc", ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(keep),
+          _ptr(Xp), _ptr(row_of), _ptr(src_of), _ptr(counts), _ptr(offsets), _stream(stream))
 
 
 def moe_expert_ffn(dtype, max_rows, d, F, n_groups, offsets, Xp, W_gu, W_down, A_save, H_save,

@@ -152,6 +152,21 @@ moe_status_t moe_permute(const moe_shape_t *shape, const void *x, const int32_t 
   return cuda_status(launch_permute(a, (cudaStream_t)stream));
 }
 
+moe_status_t moe_permute_noalloc(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
+                                 const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
+                                 int32_t *counts, int32_t *offsets, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
+  if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Xp)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > MOE_PERMUTE_NOALLOC_MAX_TOKENS) return MOE_ERR_UNSUPPORTED;
+  PermuteArgs a{};
+  a.T = shape->T; a.d = shape->d; a.E = shape->E; a.K = shape->K; a.dtype = shape->dtype;
+  a.x = x; a.topk_idx = topk_idx; a.keep = keep; a.Xp = Xp; a.row_of = row_of; a.src_of = src_of;
+  a.counts = counts; a.offsets = offsets;
+  return cuda_status(launch_permute_noalloc(a, (cudaStream_t)stream));
+}
+
 static moe_status_t ffn_check(int32_t dtype, int64_t max_rows, int32_t d, int32_t F,
                               int32_t n_groups, const int32_t *offsets, void *ws) {
   if ((dtype != MOE_F32 && dtype != MOE_BF16) || max_rows < 1 || d < 1 || F < 1 || n_groups < 1 ||

@@ -141,6 +141,7 @@ struct PermuteArgs {
   uint32_t *status;
 };
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s);
+cudaError_t launch_permute_noalloc(PermuteArgs a, cudaStream_t s);
 
 struct UnpermuteArgs {
   int64_t T;

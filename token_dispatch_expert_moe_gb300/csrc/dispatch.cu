@@ -16,6 +16,8 @@
 //      the kept tokens of expert e in the block is the popcount of the bits
 //      below t, so row_of[t,k] = base[block][e] + rank, and src_of[row] =
 //      t*K + k. Rows come out expert-major and token-ascending.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -264,6 +266,51 @@ permute_bwd_kernel(int64_t T, int d, int K, const float *__restrict__ dXp,
 }
 
 }  // namespace
+
+// ---------------------------------------------------------------------------
+// Scratch for moe_permute_noalloc: the per-block expert counts of the map
+// build live in this fixed device array instead of a caller workspace. It
+// holds MOE_PERMUTE_NOALLOC_MAX_TOKENS / 256 blocks x 64 experts (128 KB) and
+// stays resident on every GPU that loads the library until the process exits.
+// map_count writes every word that map_scan and map_scatter later read, so a
+// call never sees the previous call's counts and nothing needs clearing.
+constexpr int kNoAllocBlocks = MOE_PERMUTE_NOALLOC_MAX_TOKENS / kMapBlock;
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocBlocks * 64];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+int32_t *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_permute_scratch on the current device. In host code the
+// array's name is only a handle, so the address is looked up once per device
+// (cudaGetSymbolAddress, with that device current) and cached.
+cudaError_t permute_scratch(int32_t **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_permute_noalloc(PermuteArgs a, cudaStream_t s) {
+  if (a.T > MOE_PERMUTE_NOALLOC_MAX_TOKENS || a.E > 64) return cudaErrorInvalidValue;
+  int32_t *scratch = nullptr;
+  cudaError_t e = permute_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  a.blk_counts = scratch;
+  a.status = nullptr;  // no workspace, so no status word
+  return launch_permute(a, s);
+}
 
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   const int nblk = (int)((a.T + kMapBlock - 1) / kMapBlock);
