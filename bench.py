@@ -246,6 +246,7 @@ def main():
     w = {k: to_device(v) for k, v in inp.items() if k not in ("x", "dout")}
     layer = MoELayer(cfg_r, w)
     x = to_device(inp["x"])
+    layer.x = x   # the backward reads the forward's tokens
     dout = to_device(inp["dout"]) if cfg.backward else None
     stream = torch.cuda.current_stream()
 

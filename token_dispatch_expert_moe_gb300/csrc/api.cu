@@ -116,7 +116,14 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
   a.x = x; a.W_r = W_r; a.b_r = b_r; a.w_sg = w_sg; a.logits = logits; a.gate_logit = gate_logit;
   a.topk_idx = topk_idx; a.topk_prob = topk_prob; a.topk_w = topk_w; a.keep = keep;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_router_fused(a, s);
+  cudaError_t e;
+  if (shape->dtype == MOE_BF16 && shape->d % 64 == 0 && (w_sg == nullptr || aligned16(w_sg))) {
+    // logits on the tensor cores, then the fp32 Top-K on those logits
+    e = launch_router_tc(a, s);
+    if (e == cudaSuccess) e = launch_topk_from_logits(a, s);
+  } else {
+    e = launch_router_fused(a, s);
+  }
   if (e == cudaSuccess && shape->drop) e = launch_capacity(a, s);
   return cuda_status(e);
 }

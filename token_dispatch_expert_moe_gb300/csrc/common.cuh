@@ -126,6 +126,7 @@ struct RouteArgs {
 };
 
 cudaError_t launch_router_fused(const RouteArgs &a, cudaStream_t s);
+cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s);  // bf16, d % 64 == 0
 cudaError_t launch_topk_from_logits(const RouteArgs &a, cudaStream_t s);
 cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s);
 

@@ -24,6 +24,9 @@
 //   DX      dXp   = dA W_gu[g]                                   (B MN-major)
 //   WGD     dW_down[g] = dYp_g^T H_g     (K = the group's rows; A, B MN-major)
 //   WGU     dW_gu[g]   = dA_g^T Xp_g
+//   RT      router logits = x W_r^T (+ b_r) and gate logit x . w_sg: one
+//           group of T rows, N = E rounded up to 16 (+ 16 when the gate
+//           vector rides along as a second B box); fp32 logits out.
 // In GU/DOWN/DH/DX a tile's rows past the group's end belong to the next
 // group (or are zero-filled past the buffer); only their outputs are masked.
 // In WGD/WGU the reduction runs over the group's rows, so K rows past the end
@@ -41,7 +44,7 @@
 namespace moe {
 namespace {
 
-enum Mode { GU = 0, DOWN = 1, DH = 2, DX = 3, WGD = 4, WGU = 5 };
+enum Mode { GU = 0, DOWN = 1, DH = 2, DX = 3, WGD = 4, WGU = 5, RT = 6 };
 
 constexpr int kStages = 4;
 constexpr int BM = 128;
@@ -56,6 +59,7 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 struct TcParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
+  CUtensorMap tmC;   // RT: the gate vector w_sg as a [1, d] tensor
   int mode;
   int n_groups;
   int64_t max_rows;
@@ -68,6 +72,11 @@ struct TcParams {
   void *out0;    // GU: H; DOWN: Yp; DH: dA; DX: dXp; WG*: dW
   void *out1;    // GU: A_save (nullable)
   const void *aux;  // DH: A_save
+  // RT
+  int64_t T;
+  int E, e_pad, has_gate;
+  const float *bias;
+  float *gate_out;
   uint32_t *status;
 };
 
@@ -195,7 +204,9 @@ struct Tile {
 template <int MODE, int BN>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, const SharedState &st, int idx) {
   Tile t;
-  if constexpr (ModeTraits<MODE>::red) {
+  if constexpr (MODE == RT) {
+    t.g = 0; t.n = 0; t.m = idx; t.row0 = 0; t.rows = (int)p.T;
+  } else if constexpr (ModeTraits<MODE>::red) {
     const int MT = p.M_fixed / BM, NT = p.N / BN;
     t.g = idx / (MT * NT);
     const int loc = idx % (MT * NT);
@@ -238,7 +249,7 @@ template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using TR = ModeTraits<MODE>;
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
-  constexpr int B_BOXES = TR::b_mn ? MMA_N / 64 : MMA_N / 128;
+  constexpr int B_BOXES = TR::b_mn ? MMA_N / 64 : (MMA_N >= 128 ? MMA_N / 128 : 1);
   constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
   constexpr uint32_t kStageTx = kABytes + MMA_N * BK * 2;
   constexpr uint32_t kIdesc = instr_desc(BM, MMA_N, TR::a_mn, TR::b_mn);
@@ -254,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     st.abort = 0;
     int total = 0;
     bool bad = false;
-    if constexpr (TR::red) {
+    if constexpr (MODE == RT) {
+      total = (int)((p.T + BM - 1) / BM);
+    } else if constexpr (TR::red) {
       for (int g = 0; g < p.n_groups; ++g)
         if (p.offsets[g + 1] < p.offsets[g]) bad = true;
       total = p.n_groups * (p.M_fixed / BM) * (p.N / BN);
@@ -270,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
       st.tile_start[p.n_groups] = total;
     }
-    if (p.offsets[0] < 0 || (int64_t)p.offsets[p.n_groups] > p.max_rows) bad = true;
+    if constexpr (MODE != RT) {
+      if (p.offsets[0] < 0 || (int64_t)p.offsets[p.n_groups] > p.max_rows) bad = true;
+    }
     if (bad) {
       report(p.status, MOE_ERR_DEVICE, kInfoOffsets);
       total = 0;
@@ -332,7 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int arow = t.row0 + t.m * BM;
             tma_load_2d(sa, &p.tmA, full, kb * BK, arow);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
-            if constexpr (MODE == GU) {
+            if constexpr (MODE == RT) {
+              tma_load_2d(sb, &p.tmB, full, kb * BK, 0);
+              if (p.has_gate) tma_load_2d(sb + p.e_pad * 128, &p.tmC, full, kb * BK, 0);
+            } else if constexpr (MODE == GU) {
               tma_load_2d(sb, &p.tmB, full, kb * BK, (int)(gb + t.n * 128));
               tma_load_2d(sb + 16384, &p.tmB, full, kb * BK, (int)(gb + p.F + t.n * 128));
             } else if constexpr (TR::b_mn) {
@@ -435,7 +453,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       tc_fence_after();
       const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
       const int r_loc = t.m * BM + q * 32 + lane;
-      if constexpr (TR::red) {
+      if constexpr (MODE == RT) {
+        const int64_t row = r_loc;
+        const bool valid = row < p.T;
+        float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
+#pragma unroll 1
+        for (int c = 0; c < (BN + 31) / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int e = c * 32 + i;
+              if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[i], p.bias[e]) : v[i];
+              if (p.has_gate && e == p.e_pad) p.gate_out[row] = v[i];
+            }
+          }
+        }
+      } else if constexpr (TR::red) {
         float *out = reinterpret_cast<float *>(p.out0) + (int64_t)t.g * p.M_fixed * p.N +
                      (int64_t)r_loc * p.N + t.n * BN;
         const bool empty = t.rows <= 0;
@@ -607,6 +642,27 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
+  const int e_pad = (a.E + 15) / 16 * 16;
+  const int has_gate = a.w_sg != nullptr ? 1 : 0;
+  const int n = e_pad + 16 * has_gate;
+  TcParams p{};
+  if (!make_map(&p.tmA, a.x, a.d, a.T, 128)) return cudaErrorInvalidValue;
+  if (!make_map(&p.tmB, a.W_r, a.d, a.E, e_pad)) return cudaErrorInvalidValue;
+  if (has_gate && !make_map(&p.tmC, a.w_sg, a.d, 1, 16)) return cudaErrorInvalidValue;
+  p.mode = RT; p.n_groups = 1; p.max_rows = a.T; p.d = a.d; p.K_fixed = a.d; p.N = n;
+  p.T = a.T; p.E = a.E; p.e_pad = e_pad; p.has_gate = has_gate; p.bias = a.b_r;
+  p.out0 = a.logits; p.gate_out = a.gate_logit; p.status = a.status;
+  switch (n) {
+    case 16: return launch_mode<RT, 16>(p, s);
+    case 32: return launch_mode<RT, 32>(p, s);
+    case 48: return launch_mode<RT, 48>(p, s);
+    case 64: return launch_mode<RT, 64>(p, s);
+    case 80: return launch_mode<RT, 80>(p, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   const int d = a.d, F = a.F, E = a.n_groups;
