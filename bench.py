@@ -220,11 +220,19 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="profiling cases only: comma-separated field=value changes to the "
+                         "workload, e.g. T=4096,E=16 (the JSON line then names the changed shape)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     from synthetic import get_config, make_inputs
     cfg = get_config(args.config)
+    if args.override:
+        import dataclasses
+        kv = dict(item.split("=", 1) for item in args.override.split(","))
+        typed = {k: type(getattr(cfg, k))(v) for k, v in kv.items()}
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}[{args.override}]", **typed)
     rank, world, local = dist_env()
     dist = None
     if world > 1:

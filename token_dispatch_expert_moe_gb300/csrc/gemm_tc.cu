@@ -54,12 +54,16 @@ constexpr int kABytes = BM * BK * 2;          // 16 KB
 constexpr int kBBytesMax = 256 * BK * 2;      // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
 constexpr int kTmemCols = 512;
+constexpr int kStageOutBytes = 4096;                 // 32 rows x 128 B
+constexpr int kEpiStagingBytes = 4 * 2 * kStageOutBytes;  // 4 warps x 2 buffers
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 struct TcParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmC;   // RT: the gate vector w_sg as a [1, d] tensor
+  CUtensorMap tmO0;  // bulk-store map of out0 (box: 32 rows x 128 bytes)
+  CUtensorMap tmO1;  // bulk-store map of out1 (GU: A_save)
   int mode;
   int n_groups;
   int64_t max_rows;
@@ -169,6 +173,55 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Epilogue staging for bulk (TMA) stores. Each epilogue warp owns two 4 KB
+// buffers; a buffer holds its 32 rows x 128 bytes in the 128-byte swizzled
+// layout of the store's tensor map (16-byte chunk c of row r at chunk
+// c ^ (r % 8)), so that lane r writing its row touches every bank group once
+// per 8 lanes.
+struct Stager {
+  uint8_t *base;
+  int next;
+};
+__device__ __forceinline__ uint8_t *stage_begin(Stager &sg, int lane) {
+  // the buffer used two stores ago must have been read by its bulk copy
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+  __syncwarp();
+  uint8_t *b = sg.base + sg.next * kStageOutBytes;
+  sg.next ^= 1;
+  return b;
+}
+__device__ __forceinline__ void stage_row(uint8_t *b, int lane, const uint32_t (&w)[32]) {
+  uint8_t *row = b + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4 *>(row + ((c ^ (lane & 7)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+__device__ __forceinline__ void stage_store(uint8_t *b, const CUtensorMap *tm, int x, int y,
+                                            int lane) {
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(smem_u32(b)), "r"(x), "r"(y)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+}
+__device__ __forceinline__ void pack_f32(const float (&v)[32], uint32_t (&w)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+}
+// 32 floats -> 16 words of bf16 pairs at w[off .. off+15]
+__device__ __forceinline__ void pack_bf16(const float (&v)[32], uint32_t (&w)[32], int off) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[off + i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
 // and B (bits 7-9, 10-12 = 1), A/B major-ness (bits 15, 16: 1 = MN-major),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -257,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  SharedState &st = *reinterpret_cast<SharedState *>(smem + kStages * kStageBytes);
+  uint8_t *staging = smem + kStages * kStageBytes;
+  SharedState &st = *reinterpret_cast<SharedState *>(staging + kEpiStagingBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- set-up: tile table, barriers, TMEM
@@ -444,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     // ======================= epilogue =======================
     const int q = warp & 3;  // TMEM lane quarter of this warp
+    Stager sg{staging + (warp - 2) * 2 * kStageOutBytes, 0};
     int tcount = 0;
     for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x, ++tcount) {
       const Tile t = decode_tile<MODE, BN>(p, st, ti);
@@ -471,9 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         }
       } else if constexpr (TR::red) {
-        float *out = reinterpret_cast<float *>(p.out0) + (int64_t)t.g * p.M_fixed * p.N +
-                     (int64_t)r_loc * p.N + t.n * BN;
+        // weight-gradient tiles are always whole: bulk stores of 32 x 32 fp32
         const bool empty = t.rows <= 0;
+        const int y = t.g * p.M_fixed + t.m * BM + q * 32;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
@@ -482,9 +537,72 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
+          uint32_t w[32];
+          pack_f32(v, w);
+          uint8_t *b = stage_begin(sg, lane);
+          stage_row(b, lane, w);
+          stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
+        }
+      } else if (t.rows - t.m * BM >= BM && MODE != DH) {
+        // whole tile of one group: bulk stores (rows past the group would
+        // belong to the next group, so partial tiles take the path below)
+        const int y = t.row0 + t.m * BM + q * 32;
+        if constexpr (MODE == GU) {
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {  // 64 gate/up columns per chunk
+            uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4 *>(out + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int hh = 0; hh < 2; ++hh) {
+              float g[32], u[32];
+              tmem_ld32(tbase + c * 64 + hh * 32, g);
+              tmem_ld32(tbase + 128 + c * 64 + hh * 32, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+              pack_bf16(g, w, hh * 16);
+            }
+            uint8_t *b = stage_begin(sg, lane);
+            stage_row(b, lane, w);
+            stage_store(b, &p.tmO0, t.n * 128 + c * 64, y, lane);
+            if (p.out1 != nullptr) {
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {  // G, then U
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  float v[32];
+                  tmem_ld32(tbase + half * 128 + c * 64 + hh * 32, v);
+                  pack_bf16(v, w, hh * 16);
+                }
+                uint8_t *b2 = stage_begin(sg, lane);
+                stage_row(b2, lane, w);
+                stage_store(b2, &p.tmO1, half * p.F + t.n * 128 + c * 64, y, lane);
+              }
+            }
+          }
+        } else if constexpr (MODE == DOWN) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[32];
+              tmem_ld32(tbase + c * 64 + hh * 32, v);
+              pack_bf16(v, w, hh * 16);
+            }
+            uint8_t *b = stage_begin(sg, lane);
+            stage_row(b, lane, w);
+            stage_store(b, &p.tmO0, t.n * BN + c * 64, y, lane);
+          }
+        } else if constexpr (MODE == DX) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tbase + c * 32, v);
+            uint32_t w[32];
+            pack_f32(v, w);
+            uint8_t *b = stage_begin(sg, lane);
+            stage_row(b, lane, w);
+            stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
+          }
         }
       } else {
         const bool valid = r_loc < t.rows;
@@ -570,6 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&st.tempty[buf]));
     }
+    // every bulk store has finished before the CTA's shared memory goes away
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -613,6 +734,22 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, 
   return r == CUDA_SUCCESS;
 }
 
+// 2D tensor [outer, inner] of 2- or 4-byte elements, for bulk stores: box of
+// 128 bytes x 32 rows, 128-byte swizzle; writes outside the tensor are dropped.
+bool make_store_map(CUtensorMap *m, void *base, int esize, uint64_t inner, uint64_t outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * (uint64_t)esize};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esize), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
   static int n = 0;
   if (n == 0) {
@@ -624,7 +761,7 @@ int num_sms() {
   return n;
 }
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedState) + 1024;
+constexpr size_t kSmemBytes = kStages * kStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
 
 template <int MODE, int BN>
 cudaError_t launch_mode(const TcParams &p, cudaStream_t s) {
@@ -675,6 +812,9 @@ cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   if (!make_map(&p.tmB, a.W_gu, d, (uint64_t)E * 2 * F, 128)) return cudaErrorInvalidValue;
   p.mode = GU; p.N = F; p.K_fixed = d; p.b_group_rows = 2 * (int64_t)F;
   p.out0 = H; p.out1 = a.A_save;
+  if (!make_store_map(&p.tmO0, H, 2, F, a.max_rows)) return cudaErrorInvalidValue;
+  if (a.A_save && !make_store_map(&p.tmO1, a.A_save, 2, 2 * (uint64_t)F, a.max_rows))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_bn<GU>(p, s);
   if (e != cudaSuccess) return e;
   // DOWN
@@ -682,6 +822,7 @@ cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   if (!make_map(&q.tmA, H, F, a.max_rows, 128)) return cudaErrorInvalidValue;
   if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, 128)) return cudaErrorInvalidValue;
   q.mode = DOWN; q.N = d; q.K_fixed = F; q.b_group_rows = d; q.out0 = a.Yp; q.out1 = nullptr;
+  if (!make_store_map(&q.tmO0, a.Yp, 2, d, a.max_rows)) return cudaErrorInvalidValue;
   return launch_bn<DOWN>(q, s);
 }
 
@@ -703,6 +844,7 @@ cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
     if (!make_map(&q.tmA, a.dA, 2 * F, a.max_rows, 128)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.W_gu, d, (uint64_t)E * 2 * F, 64)) return cudaErrorInvalidValue;
     q.mode = DX; q.N = d; q.K_fixed = 2 * F; q.b_group_rows = 2 * (int64_t)F; q.out0 = a.dXp;
+    if (!make_store_map(&q.tmO0, a.dXp, 4, d, a.max_rows)) return cudaErrorInvalidValue;
     if ((e = launch_bn<DX>(q, s)) != cudaSuccess) return e;
   }
   {  // WGD: dW_down[g] = dYp_g^T H_g
@@ -710,6 +852,7 @@ cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
     if (!make_map(&q.tmA, a.dYp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.H_save, F, a.max_rows, 64)) return cudaErrorInvalidValue;
     q.mode = WGD; q.M_fixed = d; q.N = F; q.out0 = a.dW_down;
+    if (!make_store_map(&q.tmO0, a.dW_down, 4, F, (uint64_t)E * d)) return cudaErrorInvalidValue;
     if ((e = launch_bn<WGD>(q, s)) != cudaSuccess) return e;
   }
   {  // WGU: dW_gu[g] = dA_g^T Xp_g
@@ -717,6 +860,7 @@ cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
     if (!make_map(&q.tmA, a.dA, 2 * F, a.max_rows, 64)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.Xp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
     q.mode = WGU; q.M_fixed = 2 * F; q.N = d; q.out0 = a.dW_gu;
+    if (!make_store_map(&q.tmO0, a.dW_gu, 4, d, (uint64_t)E * 2 * F)) return cudaErrorInvalidValue;
     if ((e = launch_bn<WGU>(q, s)) != cudaSuccess) return e;
   }
   return cudaSuccess;

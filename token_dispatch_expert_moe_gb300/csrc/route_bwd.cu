@@ -8,8 +8,8 @@
 //      arithmetic as the forward); dp on the Top-K slots
 //      ((g - <g,w>) / Z with renorm, g without); dl = p (dp - <p,dp>).
 //   2. dx_kernel: dx_router[t] = dx_in[t] + sum_e dl[t,e] W_r[e] + dz[t] w_sg,
-//      16 tokens x 128 hidden columns per CTA, W_r slice staged in shared
-//      memory.
+//      64 tokens x 256 hidden columns per CTA, each thread's W_r column in
+//      registers.
 //   3. wgrad_partial_kernel: per chunk of tokens, partial sums of
 //      dl^T x (and dz^T x), then reduce_kernel adds the chunks in order:
 //      deterministic, no atomics.
@@ -19,10 +19,9 @@
 namespace moe {
 namespace {
 
-constexpr int kDxTok = 16;
-constexpr int kCols = 256;    // hidden columns per wgrad CTA
-constexpr int kDxCols = 128;  // hidden columns per dx CTA
-constexpr int kChunks = 16;
+constexpr int kDxTok = 64;   // tokens per dx CTA
+constexpr int kCols = 256;   // hidden columns per CTA
+constexpr int kChunks = 32;  // token chunks of the dW_r partial sums
 
 __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
   const int lane = threadIdx.x & 31;
@@ -53,24 +52,27 @@ __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
   if (v1) a.dl[t * E + lane + 32] = p1 * (dp1 - s);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kDxCols) dx_kernel(RouteBwdArgs a) {
-  __shared__ float Ws[65][kDxCols];
-  __shared__ float dls[kDxTok][65];
+// dx_router[t, j] = dx_in[t, j] + sum_c dl[t, c] W[c, j]  (row c = E is w_sg
+// with dl = dz). One thread per column j holds W[:, j] in registers for 64
+// tokens; dl rows are read from shared memory as float4 broadcasts.
+template <typename T, int CP>
+__global__ void __launch_bounds__(kCols) dx_kernel(RouteBwdArgs a) {
+  __shared__ __align__(16) float dls[kDxTok][CP];
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
   const int64_t t0 = (int64_t)blockIdx.x * kDxTok;
-  const int j0 = blockIdx.y * kDxCols;
-  const int j = j0 + threadIdx.x;
+  const int j = blockIdx.y * kCols + threadIdx.x;
   const T *W = reinterpret_cast<const T *>(a.W_r);
   const T *wsg = reinterpret_cast<const T *>(a.w_sg);
-  for (int c = 0; c < C; ++c)
-    Ws[c][threadIdx.x] = j < a.d ? to_f32(c < E ? W[(int64_t)c * a.d + j] : wsg[j]) : 0.0f;
-  for (int i = threadIdx.x; i < kDxTok * C; i += blockDim.x) {
-    const int tt = i / C, c = i % C;
+  float w[CP];
+#pragma unroll
+  for (int c = 0; c < CP; ++c)
+    w[c] = (j < a.d && c < C) ? to_f32(c < E ? W[(int64_t)c * a.d + j] : wsg[j]) : 0.0f;
+  for (int i = threadIdx.x; i < kDxTok * CP; i += blockDim.x) {
+    const int tt = i / CP, c = i % CP;
     const int64_t t = t0 + tt;
     float v = 0.0f;
-    if (t < a.T) v = c < E ? a.dl[t * E + c] : a.dz[t];
+    if (t < a.T && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
     dls[tt][c] = v;
   }
   __syncthreads();
@@ -79,47 +81,66 @@ __global__ void __launch_bounds__(kDxCols) dx_kernel(RouteBwdArgs a) {
     const int64_t t = t0 + tt;
     if (t >= a.T) break;
     float acc = a.dx_in != nullptr ? a.dx_in[t * a.d + j] : 0.0f;
-    for (int c = 0; c < C; ++c) acc = fmaf(dls[tt][c], Ws[c][threadIdx.x], acc);
+#pragma unroll
+    for (int c = 0; c < CP; c += 4) {
+      const float4 v = *reinterpret_cast<const float4 *>(&dls[tt][c]);
+      acc = fmaf(v.x, w[c], acc);
+      acc = fmaf(v.y, w[c + 1], acc);
+      acc = fmaf(v.z, w[c + 2], acc);
+      acc = fmaf(v.w, w[c + 3], acc);
+    }
     a.dx_router[t * a.d + j] = acc;
   }
 }
 
-template <typename T>
+// Partial sums over one chunk of tokens of dl^T x (and dz^T x): one thread per
+// column j keeps CP accumulators; 32 tokens of dl and x are staged in shared
+// memory per step.
+template <typename T, int CP>
 __global__ void __launch_bounds__(kCols) wgrad_partial_kernel(RouteBwdArgs a, int64_t chunk) {
-  __shared__ float dls[32][65];
+  __shared__ __align__(16) float dls[32][CP];
+  __shared__ float xs[32][kCols];
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
   const int64_t tb = (int64_t)blockIdx.x * chunk;
   const int64_t te = min(a.T, tb + chunk);
-  const int j = blockIdx.y * kCols + threadIdx.x;
+  const int j0 = blockIdx.y * kCols;
+  const int j = j0 + threadIdx.x;
   const T *x = reinterpret_cast<const T *>(a.x);
-  float acc[65];
+  float acc[CP];
 #pragma unroll
-  for (int c = 0; c < 65; ++c) acc[c] = 0.0f;
+  for (int c = 0; c < CP; ++c) acc[c] = 0.0f;
   for (int64_t s0 = tb; s0 < te; s0 += 32) {
     __syncthreads();
-    for (int i = threadIdx.x; i < 32 * C; i += blockDim.x) {
-      const int tt = i / C, c = i % C;
+    for (int i = threadIdx.x; i < 32 * CP; i += blockDim.x) {
+      const int tt = i / CP, c = i % CP;
       const int64_t t = s0 + tt;
       float v = 0.0f;
-      if (t < te) v = c < E ? a.dl[t * E + c] : a.dz[t];
+      if (t < te && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
       dls[tt][c] = v;
     }
+    for (int tt = 0; tt < 32; ++tt) {
+      const int64_t t = s0 + tt;
+      xs[tt][threadIdx.x] = (t < te && j < a.d) ? to_f32(x[t * a.d + j]) : 0.0f;
+    }
     __syncthreads();
-    if (j < a.d) {
-      const int n = (int)min((int64_t)32, te - s0);
-      for (int tt = 0; tt < n; ++tt) {
-        const float xv = to_f32(x[(s0 + tt) * a.d + j]);
+    const int n = (int)min((int64_t)32, te - s0);
+    for (int tt = 0; tt < n; ++tt) {
+      const float xv = xs[tt][threadIdx.x];
 #pragma unroll
-        for (int c = 0; c < 65; ++c)
-          if (c < C) acc[c] = fmaf(dls[tt][c], xv, acc[c]);
+      for (int c = 0; c < CP; c += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(&dls[tt][c]);
+        acc[c] = fmaf(v.x, xv, acc[c]);
+        acc[c + 1] = fmaf(v.y, xv, acc[c + 1]);
+        acc[c + 2] = fmaf(v.z, xv, acc[c + 2]);
+        acc[c + 3] = fmaf(v.w, xv, acc[c + 3]);
       }
     }
   }
   if (j >= a.d) return;
   float *part = a.partial + (int64_t)blockIdx.x * C * a.d;
 #pragma unroll
-  for (int c = 0; c < 65; ++c)
+  for (int c = 0; c < CP; ++c)
     if (c < C) part[(int64_t)c * a.d + j] = acc[c];
 }
 
@@ -153,20 +174,28 @@ size_t route_bwd_workspace_bytes(int64_t T, int d, int E) {
   return dl + (size_t)kChunks * (E + 1) * d * sizeof(float);
 }
 
-cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
-  dl_kernel<<<(unsigned)((a.T * 32 + 255) / 256), 256, 0, s>>>(a);
-  dim3 gdx((unsigned)((a.T + kDxTok - 1) / kDxTok), (unsigned)((a.d + kDxCols - 1) / kDxCols));
-  const int64_t chunk = (a.T + kChunks - 1) / kChunks;
-  const int nchunk = (int)((a.T + chunk - 1) / chunk);
+template <int CP>
+void launch_cp(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk) {
+  dim3 gdx((unsigned)((a.T + kDxTok - 1) / kDxTok), (unsigned)((a.d + kCols - 1) / kCols));
   dim3 gw((unsigned)nchunk, (unsigned)((a.d + kCols - 1) / kCols));
   if (a.dtype == MOE_BF16) {
-    dx_kernel<__nv_bfloat16><<<gdx, kDxCols, 0, s>>>(a);
-    wgrad_partial_kernel<__nv_bfloat16><<<gw, kCols, 0, s>>>(a, chunk);
+    dx_kernel<__nv_bfloat16, CP><<<gdx, kCols, 0, s>>>(a);
+    wgrad_partial_kernel<__nv_bfloat16, CP><<<gw, kCols, 0, s>>>(a, chunk);
   } else {
-    dx_kernel<float><<<gdx, kDxCols, 0, s>>>(a);
-    wgrad_partial_kernel<float><<<gw, kCols, 0, s>>>(a, chunk);
+    dx_kernel<float, CP><<<gdx, kCols, 0, s>>>(a);
+    wgrad_partial_kernel<float, CP><<<gw, kCols, 0, s>>>(a, chunk);
   }
+}
+
+cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
+  dl_kernel<<<(unsigned)((a.T * 32 + 255) / 256), 256, 0, s>>>(a);
+  const int64_t chunk = (a.T + kChunks - 1) / kChunks;
+  const int nchunk = (int)((a.T + chunk - 1) / chunk);
   const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
+  if (C <= 8) launch_cp<8>(a, s, chunk, nchunk);
+  else if (C <= 16) launch_cp<16>(a, s, chunk, nchunk);
+  else if (C <= 32) launch_cp<32>(a, s, chunk, nchunk);
+  else launch_cp<68>(a, s, chunk, nchunk);
   const int64_t n = (int64_t)C * a.d;
   reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, nchunk);
   if (a.db_r != nullptr) db_kernel<<<a.E, 1024, 0, s>>>(a);
