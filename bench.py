@@ -16,8 +16,9 @@ with its inputs in L2. SM clocks and throttle reasons are sampled with
 nvidia-smi during the timed region.
 
 `e2e` repeats the measurement through the C ABI with host buffers: each step
-copies the tokens from pinned host memory to the device and the layer output
-back, inside the timed region.
+copies its tokens from pinned host memory to the device and its output back,
+inside the timed region; the copies run on a second stream with double
+buffers, overlapping the neighbouring steps' compute.
 
 `--impl reference` times the CPU oracle (the plain numpy definition of the
 layer) on the host cores instead, on a bounded sample of the same workload.
@@ -261,8 +262,9 @@ def main():
 
     ffn_ev, perm_ev, unperm_ev = [], [], []
 
-    def step(record=False):
+    def step(x, out, record=False):
         c, s, ws = cfg_r, layer.shape, layer.ws
+        layer.x = x
         L.moe_route(s, x, w["W_r"], w.get("b_r"), w.get("w_sg"), layer.logits, layer.gate_logit,
                     layer.topk_idx, layer.topk_prob, layer.topk_w, layer.keep, ws)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
@@ -278,8 +280,7 @@ def main():
             L.moe_expert_ffn(layer.dtype_code, c.T, c.d, c.Fs, 1, layer.off1, x, w["Ws_gu"],
                              w["Ws_down"], layer.As, layer.Hs, layer.Ys, ws)
         if record: e[4].record(stream)
-        L.moe_unpermute(s, layer.Yp, layer.row_of, layer.topk_w, layer.Ys, layer.gate_logit,
-                        layer.out)
+        L.moe_unpermute(s, layer.Yp, layer.row_of, layer.topk_w, layer.Ys, layer.gate_logit, out)
         if record: e[5].record(stream)
         if c.backward:
             layer.backward(dout)
@@ -289,7 +290,7 @@ def main():
             unperm_ev.append((e[4], e[5]))
 
     for _ in range(args.warmup):
-        step()
+        step(x, layer.out)
     torch.cuda.synchronize()
     rc, info = L.moe_get_status(layer.ws)
     assert rc == 0, f"device status {rc} info {info:#x}"
@@ -302,7 +303,7 @@ def main():
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for _ in range(args.steps):
-        step(record=True)
+        step(x, layer.out, record=True)
     t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -337,23 +338,54 @@ def main():
         if ent is not None and ent.get("source_sha") == sha:   # counters of this very kernel
             traffic = ent["bytes"]
 
-    # e2e through the C ABI with host buffers
-    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_host.copy_(x)
-    out_host = torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
-    for _ in range(2):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        out_host.copy_(layer.out, non_blocking=True)
+    # e2e through the C ABI with host buffers: every step copies its tokens from
+    # pinned host memory and reads its output back; the copies run on a second
+    # stream, double-buffered, so that they overlap the neighbouring steps'
+    # compute (step i+1's input and step i-1's output move during step i).
+    copy_stream = torch.cuda.Stream()
+    x_dev = [x, torch.empty_like(x)]
+    out_dev = [layer.out, torch.empty_like(layer.out)]
+    x_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for _ in range(2)]
+    for hb in x_host:
+        hb.copy_(x)
+    out_host = [torch.empty(layer.out.shape, dtype=layer.out.dtype, pin_memory=True)
+                for _ in range(2)]
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_run(nsteps, start_event=None):
+        if start_event is not None:
+            copy_stream.wait_event(start_event)
+        with torch.cuda.stream(copy_stream):
+            x_dev[0].copy_(x_host[0], non_blocking=True)
+            h2d_done[0].record(copy_stream)
+        for i in range(nsteps):
+            b = i % 2
+            stream.wait_event(h2d_done[b])
+            if i >= 2:
+                stream.wait_event(d2h_done[b])   # out_dev[b] read back two steps ago
+            step(x_dev[b], out_dev[b])
+            comp_done[b].record(stream)
+            with torch.cuda.stream(copy_stream):
+                if i + 1 < nsteps:
+                    nb = (i + 1) % 2
+                    if i >= 1:
+                        copy_stream.wait_event(comp_done[nb])   # step i-1 done with x_dev[nb]
+                    x_dev[nb].copy_(x_host[nb], non_blocking=True)
+                    h2d_done[nb].record(copy_stream)
+                copy_stream.wait_event(comp_done[b])
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+                d2h_done[b].record(copy_stream)
+        stream.wait_stream(copy_stream)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        x.copy_(x_host, non_blocking=True)
-        step()
-        out_host.copy_(layer.out, non_blocking=True)
+    e2e_run(args.steps, start_event=e0)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e = aggregate(cfg.T * args.steps, e0.elapsed_time(e1) / 1e3, world, dist)

@@ -242,6 +242,7 @@ struct SharedState {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t ebar[4];  // DH: per-epilogue-warp A_save box loads
   uint32_t tmem_base;
   volatile int abort;
   int total_tiles;
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(smem_u32(&st.tempty[b]), 4);
     }
     mbar_init(smem_u32(&st.drain), 1);
+    for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&st.ebar[w]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
@@ -499,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ======================= epilogue =======================
     const int q = warp & 3;  // TMEM lane quarter of this warp
     Stager sg{staging + (warp - 2) * 2 * kStageOutBytes, 0};
+    uint32_t ephase = 0;  // DH: parity of this warp's A_save load barrier
     int tcount = 0;
     for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x, ++tcount) {
       const Tile t = decode_tile<MODE, BN>(p, st, ti);
@@ -543,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           stage_row(b, lane, w);
           stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
         }
-      } else if (t.rows - t.m * BM >= BM && MODE != DH) {
+      } else if (t.rows - t.m * BM >= BM) {
         // whole tile of one group: bulk stores (rows past the group would
         // belong to the next group, so partial tiles take the path below)
         const int y = t.row0 + t.m * BM + q * 32;
@@ -602,6 +605,58 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             uint8_t *b = stage_begin(sg, lane);
             stage_row(b, lane, w);
             stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
+          }
+        } else if constexpr (MODE == DH) {
+          // per 64 columns: TMA-load this warp's 32 rows of G and U from
+          // A_save into the two staging buffers, turn them into dG and dU in
+          // place, bulk-store both halves of dA
+          uint8_t *bg = sg.base, *bu = sg.base + kStageOutBytes;
+          const uint32_t ebar = smem_u32(&st.ebar[warp - 2]);
+          bool ok = true;
+#pragma unroll 1
+          for (int c = 0; c < BN / 64 && ok; ++c) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              mbar_expect_tx(ebar, 2 * kStageOutBytes);
+              tma_load_2d(smem_u32(bg), &p.tmO1, ebar, t.n * BN + c * 64, y);
+              tma_load_2d(smem_u32(bu), &p.tmO1, ebar, p.F + t.n * BN + c * 64, y);
+            }
+            ok = __all_sync(0xffffffffu, wait_bounded(st, ebar, ephase, p.status, 5));
+            ephase ^= 1;
+            if (!ok) break;
+            float dh[64];
+            tmem_ld32(tbase + c * 64, *reinterpret_cast<float(*)[32]>(dh));
+            tmem_ld32(tbase + c * 64 + 32, *reinterpret_cast<float(*)[32]>(dh + 32));
+            uint8_t *rg = bg + lane * 128, *ru = bu + lane * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch = columns 8ch..8ch+7
+              const int off = (ch ^ (lane & 7)) << 4;
+              float G[8], U[8], dG[8], dU[8];
+              load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(rg + off), G);
+              load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float sgm = 1.0f / (1.0f + __expf(-G[j]));
+                dG[j] = dh[8 * ch + j] * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
+                dU[j] = dh[8 * ch + j] * G[j] * sgm;
+              }
+              store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(rg + off), dG);
+              store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(ru + off), dU);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                               reinterpret_cast<uint64_t>(&p.tmO0)),
+                           "r"(smem_u32(bg)), "r"(t.n * BN + c * 64), "r"(y)
+                           : "memory");
+              asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                               reinterpret_cast<uint64_t>(&p.tmO0)),
+                           "r"(smem_u32(bu)), "r"(p.F + t.n * BN + c * 64), "r"(y)
+                           : "memory");
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
           }
         }
       } else {
@@ -837,6 +892,9 @@ cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
     if (!make_map(&q.tmA, a.dYp, d, a.max_rows, 128)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, 64)) return cudaErrorInvalidValue;
     q.mode = DH; q.N = F; q.K_fixed = d; q.b_group_rows = d; q.out0 = a.dA; q.aux = a.A_save;
+    if (!make_store_map(&q.tmO0, a.dA, 2, 2 * (uint64_t)F, a.max_rows)) return cudaErrorInvalidValue;
+    if (!make_store_map(&q.tmO1, const_cast<void *>(a.A_save), 2, 2 * (uint64_t)F, a.max_rows))
+      return cudaErrorInvalidValue;
     if ((e = launch_bn<DH>(q, s)) != cudaSuccess) return e;
   }
   {  // DX: dXp = dA W_gu

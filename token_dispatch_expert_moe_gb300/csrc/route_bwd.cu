@@ -77,19 +77,31 @@ __global__ void __launch_bounds__(kCols) dx_kernel(RouteBwdArgs a) {
   }
   __syncthreads();
   if (j >= a.d) return;
-  for (int tt = 0; tt < kDxTok; ++tt) {
+  // two tokens at a time, four partial sums each (combined in a fixed order)
+  for (int tt = 0; tt < kDxTok; tt += 2) {
     const int64_t t = t0 + tt;
     if (t >= a.T) break;
-    float acc = a.dx_in != nullptr ? a.dx_in[t * a.d + j] : 0.0f;
+    const bool two = t + 1 < a.T;
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < CP; c += 4) {
       const float4 v = *reinterpret_cast<const float4 *>(&dls[tt][c]);
-      acc = fmaf(v.x, w[c], acc);
-      acc = fmaf(v.y, w[c + 1], acc);
-      acc = fmaf(v.z, w[c + 2], acc);
-      acc = fmaf(v.w, w[c + 3], acc);
+      const float4 u = *reinterpret_cast<const float4 *>(&dls[tt + 1][c]);
+      p0[0] = fmaf(v.x, w[c], p0[0]);
+      p0[1] = fmaf(v.y, w[c + 1], p0[1]);
+      p0[2] = fmaf(v.z, w[c + 2], p0[2]);
+      p0[3] = fmaf(v.w, w[c + 3], p0[3]);
+      p1[0] = fmaf(u.x, w[c], p1[0]);
+      p1[1] = fmaf(u.y, w[c + 1], p1[1]);
+      p1[2] = fmaf(u.z, w[c + 2], p1[2]);
+      p1[3] = fmaf(u.w, w[c + 3], p1[3]);
     }
-    a.dx_router[t * a.d + j] = acc;
+    const float in0 = a.dx_in != nullptr ? a.dx_in[t * a.d + j] : 0.0f;
+    a.dx_router[t * a.d + j] = in0 + ((p0[0] + p0[1]) + (p0[2] + p0[3]));
+    if (two) {
+      const float in1 = a.dx_in != nullptr ? a.dx_in[(t + 1) * a.d + j] : 0.0f;
+      a.dx_router[(t + 1) * a.d + j] = in1 + ((p1[0] + p1[1]) + (p1[2] + p1[3]));
+    }
   }
 }
 
@@ -119,6 +131,7 @@ __global__ void __launch_bounds__(kCols) wgrad_partial_kernel(RouteBwdArgs a, in
       if (t < te && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
       dls[tt][c] = v;
     }
+#pragma unroll 8
     for (int tt = 0; tt < 32; ++tt) {
       const int64_t t = s0 + tt;
       xs[tt][threadIdx.x] = (t < te && j < a.d) ? to_f32(x[t * a.d + j]) : 0.0f;
