@@ -123,3 +123,21 @@ def test_ffn_backward_group_layouts(rows, dtype):
     rnd = O.act_rounder(dtype, True)
     dYp = rnd(O.decode(gen(6, 104, (n, d))) * 0.5)
     _check_bwd(L, dtype, Xp, offsets, W_gu, W_down, dYp, d, F)
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_single_cta_and_pair_kernels_agree(pair):
+    """The CTA-pair and single-CTA grouped GEMMs both match the oracle (each
+    run in its own process, since the kernel choice is read once)."""
+    import os
+    import subprocess
+    import sys
+    lib()
+    code = ("import sys; sys.argv=['x']; import pytest; "
+            "sys.exit(pytest.main(['-q', '-p', 'no:cacheprovider', '-k', "
+            "'group_layouts and bf16', 'tests/test_gpu_ffn.py']))")
+    env = dict(os.environ, MOE_GEMM_PAIR=pair)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]

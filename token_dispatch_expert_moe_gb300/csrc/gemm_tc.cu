@@ -36,6 +36,8 @@
 // %globaltimer); on expiry the kernel records MOE_ERR_TIMEOUT in the status
 // word, tells the other roles to stop, drains what it has in flight and
 // returns, so the GPU context stays usable.
+#include <cstdlib>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -146,6 +148,57 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                    bar)
                : "memory");
 }
+// --- CTA-pair (cta_group::2) forms -------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// TMA load into this CTA's shared memory that completes on a barrier of
+// either CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the barrier at this shared-memory offset in both CTAs of the pair
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -236,9 +289,10 @@ template <int MODE> struct ModeTraits {
   static constexpr int b_mn = (MODE == DH || MODE == DX || red) ? 1 : 0;
 };
 
+constexpr int kMaxStages = 6;
 struct SharedState {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -295,6 +349,243 @@ __device__ bool wait_bounded(SharedState &st, uint32_t bar, uint32_t parity, uin
       report(status, MOE_ERR_TIMEOUT, kInfoGemmTimeout + role);
       st.abort = 1;
       return false;
+    }
+  }
+}
+
+// One tile's epilogue for the epilogue warp that owns TMEM lane quarter q.
+template <int MODE, int BN>
+__device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st, Stager &sg,
+                                              uint32_t &ephase, const Tile &t, uint32_t tbase,
+                                              int q, int warp, int lane) {
+  using TR = ModeTraits<MODE>;
+  const int r_loc = t.m * BM + q * 32 + lane;
+  if constexpr (MODE == RT) {
+    const int64_t row = r_loc;
+    const bool valid = row < p.T;
+    float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
+#pragma unroll 1
+    for (int c = 0; c < (BN + 31) / 32; ++c) {
+      float v[32];
+      tmem_ld32(tbase + c * 32, v);
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c * 32 + i;
+          if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[i], p.bias[e]) : v[i];
+          if (p.has_gate && e == p.e_pad) p.gate_out[row] = v[i];
+        }
+      }
+    }
+  } else if constexpr (TR::red) {
+    // weight-gradient tiles are always whole: bulk stores of 32 x 32 fp32
+    const bool empty = t.rows <= 0;
+    const int y = t.g * p.M_fixed + t.m * BM + q * 32;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tbase + c * 32, v);
+      if (empty) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      }
+      uint32_t w[32];
+      pack_f32(v, w);
+      uint8_t *b = stage_begin(sg, lane);
+      stage_row(b, lane, w);
+      stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
+    }
+  } else if (t.rows - t.m * BM >= BM) {
+    // whole tile of one group: bulk stores (rows past the group would
+    // belong to the next group, so partial tiles take the path below)
+    const int y = t.row0 + t.m * BM + q * 32;
+    if constexpr (MODE == GU) {
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {  // 64 gate/up columns per chunk
+        uint32_t w[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float g[32], u[32];
+          tmem_ld32(tbase + c * 64 + hh * 32, g);
+          tmem_ld32(tbase + 128 + c * 64 + hh * 32, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+          pack_bf16(g, w, hh * 16);
+        }
+        uint8_t *b = stage_begin(sg, lane);
+        stage_row(b, lane, w);
+        stage_store(b, &p.tmO0, t.n * 128 + c * 64, y, lane);
+        if (p.out1 != nullptr) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {  // G, then U
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[32];
+              tmem_ld32(tbase + half * 128 + c * 64 + hh * 32, v);
+              pack_bf16(v, w, hh * 16);
+            }
+            uint8_t *b2 = stage_begin(sg, lane);
+            stage_row(b2, lane, w);
+            stage_store(b2, &p.tmO1, half * p.F + t.n * 128 + c * 64, y, lane);
+          }
+        }
+      }
+    } else if constexpr (MODE == DOWN) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[32];
+          tmem_ld32(tbase + c * 64 + hh * 32, v);
+          pack_bf16(v, w, hh * 16);
+        }
+        uint8_t *b = stage_begin(sg, lane);
+        stage_row(b, lane, w);
+        stage_store(b, &p.tmO0, t.n * BN + c * 64, y, lane);
+      }
+    } else if constexpr (MODE == DX) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        uint32_t w[32];
+        pack_f32(v, w);
+        uint8_t *b = stage_begin(sg, lane);
+        stage_row(b, lane, w);
+        stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
+      }
+    } else if constexpr (MODE == DH) {
+      // per 64 columns: TMA-load this warp's 32 rows of G and U from
+      // A_save into the two staging buffers, turn them into dG and dU in
+      // place, bulk-store both halves of dA
+      uint8_t *bg = sg.base, *bu = sg.base + kStageOutBytes;
+      const uint32_t ebar = smem_u32(&st.ebar[warp - 2]);
+      bool ok = true;
+#pragma unroll 1
+      for (int c = 0; c < BN / 64 && ok; ++c) {
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(ebar, 2 * kStageOutBytes);
+          tma_load_2d(smem_u32(bg), &p.tmO1, ebar, t.n * BN + c * 64, y);
+          tma_load_2d(smem_u32(bu), &p.tmO1, ebar, p.F + t.n * BN + c * 64, y);
+        }
+        ok = __all_sync(0xffffffffu, wait_bounded(st, ebar, ephase, p.status, 5));
+        ephase ^= 1;
+        if (!ok) break;
+        float dh[64];
+        tmem_ld32(tbase + c * 64, *reinterpret_cast<float(*)[32]>(dh));
+        tmem_ld32(tbase + c * 64 + 32, *reinterpret_cast<float(*)[32]>(dh + 32));
+        uint8_t *rg = bg + lane * 128, *ru = bu + lane * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch = columns 8ch..8ch+7
+          const int off = (ch ^ (lane & 7)) << 4;
+          float G[8], U[8], dG[8], dU[8];
+          load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(rg + off), G);
+          load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float sgm = 1.0f / (1.0f + __expf(-G[j]));
+            dG[j] = dh[8 * ch + j] * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
+            dU[j] = dh[8 * ch + j] * G[j] * sgm;
+          }
+          store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(rg + off), dG);
+          store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(ru + off), dU);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                           reinterpret_cast<uint64_t>(&p.tmO0)),
+                       "r"(smem_u32(bg)), "r"(t.n * BN + c * 64), "r"(y)
+                       : "memory");
+          asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                           reinterpret_cast<uint64_t>(&p.tmO0)),
+                       "r"(smem_u32(bu)), "r"(p.F + t.n * BN + c * 64), "r"(y)
+                       : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+    }
+  } else {
+    const bool valid = r_loc < t.rows;
+    const int64_t row = (int64_t)t.row0 + r_loc;
+    if constexpr (MODE == GU) {
+      __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.F + t.n * 128;
+      __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(p.out1);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float g[32], u[32];
+        tmem_ld32(tbase + c * 32, g);
+        tmem_ld32(tbase + 128 + c * 32, u);
+        if (valid) {
+          float h[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            store16<__nv_bfloat16>(H + c * 32 + i, *reinterpret_cast<float(*)[8]>(h + i));
+          }
+          if (As != nullptr) {
+            __nv_bfloat16 *ag = As + row * 2 * p.F + t.n * 128 + c * 32;
+            __nv_bfloat16 *au = ag + p.F;
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              store16<__nv_bfloat16>(ag + i, *reinterpret_cast<float(*)[8]>(g + i));
+              store16<__nv_bfloat16>(au + i, *reinterpret_cast<float(*)[8]>(u + i));
+            }
+          }
+        }
+      }
+    } else if constexpr (MODE == DOWN) {
+      __nv_bfloat16 *Y = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.N + t.n * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8)
+            store16<__nv_bfloat16>(Y + c * 32 + i, *reinterpret_cast<float(*)[8]>(v + i));
+        }
+      }
+    } else if constexpr (MODE == DH) {
+      const __nv_bfloat16 *As = reinterpret_cast<const __nv_bfloat16 *>(p.aux) + row * 2 * p.F + t.n * BN;
+      __nv_bfloat16 *dA = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * 2 * p.F + t.n * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float dh[32];
+        tmem_ld32(tbase + c * 32, dh);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            float G[8], U[8], dG[8], dU[8];
+            load16<__nv_bfloat16>(As + c * 32 + i, G);
+            load16<__nv_bfloat16>(As + p.F + c * 32 + i, U);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float sg = 1.0f / (1.0f + __expf(-G[j]));
+              dG[j] = dh[i + j] * U[j] * sg * (1.0f + G[j] * (1.0f - sg));
+              dU[j] = dh[i + j] * G[j] * sg;
+            }
+            store16<__nv_bfloat16>(dA + c * 32 + i, dG);
+            store16<__nv_bfloat16>(dA + p.F + c * 32 + i, dU);
+          }
+        }
+      }
+    } else {  // DX
+      float *o = reinterpret_cast<float *>(p.out0) + row * p.N + t.n * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(o + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
     }
   }
 }
@@ -510,235 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
-      const int r_loc = t.m * BM + q * 32 + lane;
-      if constexpr (MODE == RT) {
-        const int64_t row = r_loc;
-        const bool valid = row < p.T;
-        float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
-#pragma unroll 1
-        for (int c = 0; c < (BN + 31) / 32; ++c) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-          if (valid) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int e = c * 32 + i;
-              if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[i], p.bias[e]) : v[i];
-              if (p.has_gate && e == p.e_pad) p.gate_out[row] = v[i];
-            }
-          }
-        }
-      } else if constexpr (TR::red) {
-        // weight-gradient tiles are always whole: bulk stores of 32 x 32 fp32
-        const bool empty = t.rows <= 0;
-        const int y = t.g * p.M_fixed + t.m * BM + q * 32;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-          if (empty) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-          }
-          uint32_t w[32];
-          pack_f32(v, w);
-          uint8_t *b = stage_begin(sg, lane);
-          stage_row(b, lane, w);
-          stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
-        }
-      } else if (t.rows - t.m * BM >= BM) {
-        // whole tile of one group: bulk stores (rows past the group would
-        // belong to the next group, so partial tiles take the path below)
-        const int y = t.row0 + t.m * BM + q * 32;
-        if constexpr (MODE == GU) {
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {  // 64 gate/up columns per chunk
-            uint32_t w[32];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              float g[32], u[32];
-              tmem_ld32(tbase + c * 64 + hh * 32, g);
-              tmem_ld32(tbase + 128 + c * 64 + hh * 32, u);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
-              pack_bf16(g, w, hh * 16);
-            }
-            uint8_t *b = stage_begin(sg, lane);
-            stage_row(b, lane, w);
-            stage_store(b, &p.tmO0, t.n * 128 + c * 64, y, lane);
-            if (p.out1 != nullptr) {
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {  // G, then U
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                  float v[32];
-                  tmem_ld32(tbase + half * 128 + c * 64 + hh * 32, v);
-                  pack_bf16(v, w, hh * 16);
-                }
-                uint8_t *b2 = stage_begin(sg, lane);
-                stage_row(b2, lane, w);
-                stage_store(b2, &p.tmO1, half * p.F + t.n * 128 + c * 64, y, lane);
-              }
-            }
-          }
-        } else if constexpr (MODE == DOWN) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 64; ++c) {
-            uint32_t w[32];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              float v[32];
-              tmem_ld32(tbase + c * 64 + hh * 32, v);
-              pack_bf16(v, w, hh * 16);
-            }
-            uint8_t *b = stage_begin(sg, lane);
-            stage_row(b, lane, w);
-            stage_store(b, &p.tmO0, t.n * BN + c * 64, y, lane);
-          }
-        } else if constexpr (MODE == DX) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(tbase + c * 32, v);
-            uint32_t w[32];
-            pack_f32(v, w);
-            uint8_t *b = stage_begin(sg, lane);
-            stage_row(b, lane, w);
-            stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
-          }
-        } else if constexpr (MODE == DH) {
-          // per 64 columns: TMA-load this warp's 32 rows of G and U from
-          // A_save into the two staging buffers, turn them into dG and dU in
-          // place, bulk-store both halves of dA
-          uint8_t *bg = sg.base, *bu = sg.base + kStageOutBytes;
-          const uint32_t ebar = smem_u32(&st.ebar[warp - 2]);
-          bool ok = true;
-#pragma unroll 1
-          for (int c = 0; c < BN / 64 && ok; ++c) {
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-              mbar_expect_tx(ebar, 2 * kStageOutBytes);
-              tma_load_2d(smem_u32(bg), &p.tmO1, ebar, t.n * BN + c * 64, y);
-              tma_load_2d(smem_u32(bu), &p.tmO1, ebar, p.F + t.n * BN + c * 64, y);
-            }
-            ok = __all_sync(0xffffffffu, wait_bounded(st, ebar, ephase, p.status, 5));
-            ephase ^= 1;
-            if (!ok) break;
-            float dh[64];
-            tmem_ld32(tbase + c * 64, *reinterpret_cast<float(*)[32]>(dh));
-            tmem_ld32(tbase + c * 64 + 32, *reinterpret_cast<float(*)[32]>(dh + 32));
-            uint8_t *rg = bg + lane * 128, *ru = bu + lane * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch = columns 8ch..8ch+7
-              const int off = (ch ^ (lane & 7)) << 4;
-              float G[8], U[8], dG[8], dU[8];
-              load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(rg + off), G);
-              load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float sgm = 1.0f / (1.0f + __expf(-G[j]));
-                dG[j] = dh[8 * ch + j] * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
-                dU[j] = dh[8 * ch + j] * G[j] * sgm;
-              }
-              store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(rg + off), dG);
-              store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(ru + off), dU);
-            }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
-              asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                               reinterpret_cast<uint64_t>(&p.tmO0)),
-                           "r"(smem_u32(bg)), "r"(t.n * BN + c * 64), "r"(y)
-                           : "memory");
-              asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                               reinterpret_cast<uint64_t>(&p.tmO0)),
-                           "r"(smem_u32(bu)), "r"(p.F + t.n * BN + c * 64), "r"(y)
-                           : "memory");
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            }
-          }
-        }
-      } else {
-        const bool valid = r_loc < t.rows;
-        const int64_t row = (int64_t)t.row0 + r_loc;
-        if constexpr (MODE == GU) {
-          __nv_bfloat16 *H = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.F + t.n * 128;
-          __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(p.out1);
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float g[32], u[32];
-            tmem_ld32(tbase + c * 32, g);
-            tmem_ld32(tbase + 128 + c * 32, u);
-            if (valid) {
-              float h[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
-#pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                store16<__nv_bfloat16>(H + c * 32 + i, *reinterpret_cast<float(*)[8]>(h + i));
-              }
-              if (As != nullptr) {
-                __nv_bfloat16 *ag = As + row * 2 * p.F + t.n * 128 + c * 32;
-                __nv_bfloat16 *au = ag + p.F;
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                  store16<__nv_bfloat16>(ag + i, *reinterpret_cast<float(*)[8]>(g + i));
-                  store16<__nv_bfloat16>(au + i, *reinterpret_cast<float(*)[8]>(u + i));
-                }
-              }
-            }
-          }
-        } else if constexpr (MODE == DOWN) {
-          __nv_bfloat16 *Y = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * p.N + t.n * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(tbase + c * 32, v);
-            if (valid) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 8)
-                store16<__nv_bfloat16>(Y + c * 32 + i, *reinterpret_cast<float(*)[8]>(v + i));
-            }
-          }
-        } else if constexpr (MODE == DH) {
-          const __nv_bfloat16 *As = reinterpret_cast<const __nv_bfloat16 *>(p.aux) + row * 2 * p.F + t.n * BN;
-          __nv_bfloat16 *dA = reinterpret_cast<__nv_bfloat16 *>(p.out0) + row * 2 * p.F + t.n * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float dh[32];
-            tmem_ld32(tbase + c * 32, dh);
-            if (valid) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 8) {
-                float G[8], U[8], dG[8], dU[8];
-                load16<__nv_bfloat16>(As + c * 32 + i, G);
-                load16<__nv_bfloat16>(As + p.F + c * 32 + i, U);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float sg = 1.0f / (1.0f + __expf(-G[j]));
-                  dG[j] = dh[i + j] * U[j] * sg * (1.0f + G[j] * (1.0f - sg));
-                  dU[j] = dh[i + j] * G[j] * sg;
-                }
-                store16<__nv_bfloat16>(dA + c * 32 + i, dG);
-                store16<__nv_bfloat16>(dA + p.F + c * 32 + i, dU);
-              }
-            }
-          }
-        } else {  // DX
-          float *o = reinterpret_cast<float *>(p.out0) + row * p.N + t.n * BN;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(tbase + c * 32, v);
-            if (valid) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 4)
-                *reinterpret_cast<float4 *>(o + c * 32 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-            }
-          }
-        }
-      }
+      epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&st.tempty[buf]));
@@ -753,6 +816,219 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant of the row-grouped modes (GU, DOWN, DH, DX): a cluster of
+// two CTAs computes a 256-row tile. Each CTA holds its own 128 rows of A and
+// half of B's columns; the even CTA issues M=256 tcgen05.mma.cta_group::2,
+// which reads both halves and writes each CTA's 128 accumulator rows into
+// that CTA's TMEM. Per SM this halves the B operand traffic per FLOP, so a
+// 6-stage ring of 32 KB stages covers more latency at a lower data rate.
+//   producer (both CTAs): own A box + own B half, completing on the even
+//     CTA's full barrier (which expects both CTAs' bytes);
+//   MMA (even CTA only): commits multicast to both CTAs' empty / tfull;
+//   epilogue (both CTAs): own TMEM rows, then arrive on the even CTA's tempty
+//     (8 arrivals: 4 warps x 2 CTAs).
+constexpr int kPairStages = 6;
+constexpr int kPairStageBytes = 32768;
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+  static_assert(MODE == GU || MODE == DOWN || MODE == DH || MODE == DX, "row-grouped modes only");
+  using TR = ModeTraits<MODE>;
+  constexpr int MMA_N = (MODE == GU) ? 256 : BN;
+  constexpr int HALF_N = MMA_N / 2;
+  constexpr uint32_t kTx = 2u * (kABytes + HALF_N * BK * 2);
+  constexpr uint32_t kIdesc = instr_desc(256, MMA_N, TR::a_mn, TR::b_mn);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *staging = smem + kPairStages * kPairStageBytes;
+  SharedState &st = *reinterpret_cast<SharedState *>(staging + kEpiStagingBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    st.abort = 0;
+    int total = 0;
+    bool bad = false;
+    const int NT = p.N / (MODE == GU ? 128 : BN);
+    for (int g = 0; g < p.n_groups; ++g) {
+      const int rows = p.offsets[g + 1] - p.offsets[g];
+      if (rows < 0) bad = true;
+      const int mt = rows > 0 ? (rows + 255) / 256 : 0;   // 256-row pair tiles
+      st.tile_start[g] = total;
+      st.mtiles[g] = mt > 0 ? mt : 1;
+      total += mt * NT;
+    }
+    st.tile_start[p.n_groups] = total;
+    if (p.offsets[0] < 0 || (int64_t)p.offsets[p.n_groups] > p.max_rows) bad = true;
+    if (bad) {
+      report(p.status, MOE_ERR_DEVICE, kInfoOffsets);
+      total = 0;
+    }
+    st.total_tiles = total;
+    for (int i = 0; i < kPairStages; ++i) {
+      mbar_init(smem_u32(&st.full[i]), 1);
+      mbar_init(smem_u32(&st.empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&st.tfull[b]), 1);
+      mbar_init(smem_u32(&st.tempty[b]), 8);
+    }
+    mbar_init(smem_u32(&st.drain), 1);
+    for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&st.ebar[w]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&st.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers initialised before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem = st.tmem_base;
+  const int total = st.total_tiles;
+
+  if (warp == 0) {
+    // ======================= TMA producer (both CTAs) =======================
+    if (lane == 0) {
+      int it = 0;
+      int last_phase[kPairStages];
+#pragma unroll
+      for (int i = 0; i < kPairStages; ++i) last_phase[i] = -1;
+      for (int pt = cid; pt < total && !st.abort; pt += ncl) {
+        Tile t = decode_tile<MODE, BN>(p, st, pt);
+        t.m = 2 * t.m + (int)rank;
+        const int kblocks = p.K_fixed / BK;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1;
+          if (!wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 1)) break;
+          const uint32_t full_leader = map_to_cta(smem_u32(&st.full[s]), 0);
+          if (leader) mbar_expect_tx(smem_u32(&st.full[s]), kTx);
+          last_phase[s] = (int)ph;
+          const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
+          const uint32_t sb = sa + kABytes;
+          tma_load_2d_pair(sa, &p.tmA, full_leader, kb * BK, t.row0 + t.m * BM);
+          const int64_t gb = (int64_t)t.g * p.b_group_rows;
+          if constexpr (MODE == GU) {   // even CTA: gate rows, odd CTA: up rows
+            tma_load_2d_pair(sb, &p.tmB, full_leader, kb * BK,
+                             (int)(gb + (int64_t)rank * p.F + t.n * 128));
+          } else if constexpr (TR::b_mn) {
+#pragma unroll
+            for (int b = 0; b < HALF_N / 64; ++b)
+              tma_load_2d_pair(sb + b * 8192, &p.tmB, full_leader,
+                               t.n * BN + (int)rank * HALF_N + 64 * b, (int)(gb + kb * BK));
+          } else {
+            tma_load_2d_pair(sb, &p.tmB, full_leader, kb * BK,
+                             (int)(gb + t.n * BN + (int)rank * HALF_N));
+          }
+        }
+      }
+      // the even CTA's full barriers see both CTAs' loads land
+      if (leader) {
+        for (int i = 0; i < kPairStages; ++i)
+          if (last_phase[i] >= 0) {
+            const uint32_t bar = smem_u32(&st.full[i]);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(bar, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (even CTA) =======================
+    if (leader) {
+      int it = 0, tcount = 0;
+      bool issued_any = false;
+      for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
+        const int kblocks = p.K_fixed / BK;
+        const int buf = tcount & 1;
+        const uint32_t use = (tcount >> 1) & 1;
+        if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2))) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem + buf * 256;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kPairStages;
+          const uint32_t ph = (it / kPairStages) & 1;
+          if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
+            const uint32_t sb = sa + kABytes;
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks) {
+              const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
+              uint64_t bd;
+              if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
+              else bd = smem_desc(sb + ks * 32, 16, 1024);
+              tc_mma_pair(dcol, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_both(smem_u32(&st.empty[s]));
+            issued_any = true;
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair_both(smem_u32(&st.tfull[buf]));
+        __syncwarp();
+      }
+      if (lane == 0 && issued_any) {
+        tc_commit_pair_local(smem_u32(&st.drain));
+        const uint32_t bar = smem_u32(&st.drain);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(bar, 0) && globaltimer() - t0 < kTimeoutNs) {
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    // ======================= epilogue (both CTAs) =======================
+    const int q = warp & 3;
+    Stager sg{staging + (warp - 2) * 2 * kStageOutBytes, 0};
+    uint32_t ephase = 0;
+    int tcount = 0;
+    for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
+      Tile t = decode_tile<MODE, BN>(p, st, pt);
+      t.m = 2 * t.m + (int)rank;
+      const int buf = tcount & 1;
+      const uint32_t use = (tcount >> 1) & 1;
+      if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
+      epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&st.tempty[buf]), 0));
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // no cross-CTA traffic after this point
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -827,10 +1103,47 @@ cudaError_t launch_mode(const TcParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+constexpr size_t kPairSmemBytes =
+    kPairStages * kPairStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
+
+template <int MODE, int BN>
+cudaError_t launch_pair(const TcParams &p, cudaStream_t s) {
+  auto k = tc_gemm_pair_kernel<MODE, BN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+// The row-grouped modes run as CTA pairs; MOE_GEMM_PAIR=0 selects the
+// single-CTA kernels instead (kept for comparison).
+bool pair_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char *e = getenv("MOE_GEMM_PAIR");
+    v = (e != nullptr && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
 template <int MODE>
 cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
-  if (MODE == GU || p.N % 256 != 0) return launch_mode<MODE, 128>(p, s);
-  return launch_mode<MODE, 256>(p, s);
+  const bool bn256 = !(MODE == GU || p.N % 256 != 0);
+  if constexpr (MODE == GU || MODE == DOWN || MODE == DH || MODE == DX) {
+    if (pair_enabled()) return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
+  }
+  return bn256 ? launch_mode<MODE, 256>(p, s) : launch_mode<MODE, 128>(p, s);
 }
 
 }  // namespace
@@ -875,7 +1188,9 @@ cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   // DOWN
   TcParams q = p;
   if (!make_map(&q.tmA, H, F, a.max_rows, 128)) return cudaErrorInvalidValue;
-  if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, 128)) return cudaErrorInvalidValue;
+  // the pair kernel's CTAs each load half of a B tile of 128 or 256 rows
+  const uint32_t down_box = pair_enabled() ? (d % 256 == 0 ? 128 : 64) : 128;
+  if (!make_map(&q.tmB, a.W_down, F, (uint64_t)E * d, down_box)) return cudaErrorInvalidValue;
   q.mode = DOWN; q.N = d; q.K_fixed = F; q.b_group_rows = d; q.out0 = a.Yp; q.out1 = nullptr;
   if (!make_store_map(&q.tmO0, a.Yp, 2, d, a.max_rows)) return cudaErrorInvalidValue;
   return launch_bn<DOWN>(q, s);
