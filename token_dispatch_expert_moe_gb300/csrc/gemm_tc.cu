@@ -110,6 +110,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -297,6 +308,8 @@ struct SharedState {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t ebar[4];  // DH: per-epilogue-warp A_save box loads
+  uint64_t zfull[kMaxStages];   // pair WG*: odd CTA's own ragged-block loads
+  uint64_t zready[kMaxStages];  // pair WG*: odd CTA has zeroed its tail rows
   uint32_t tmem_base;
   volatile int abort;
   int total_tiles;
@@ -590,6 +603,38 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
   }
 }
 
+// bounded wait with cluster-scope acquire (signals that come from the peer CTA)
+__device__ bool wait_bounded_cluster(SharedState &st, uint32_t bar, uint32_t parity,
+                                     uint32_t *status, uint32_t role) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (st.abort) return false;
+    if (globaltimer() - t0 > kTimeoutNs) {
+      report(status, MOE_ERR_TIMEOUT, kInfoGemmTimeout + role);
+      st.abort = 1;
+      return false;
+    }
+  }
+}
+
+// Zero K rows [valid, 64) of a stage's boxes: A_BOXES boxes of A at sa,
+// B_BOXES boxes of B at sa + kABytes (MN-major boxes: 64 K rows x 128 B).
+template <int A_BOXES, int B_BOXES>
+__device__ __forceinline__ void zero_tail_rows(uint8_t *sa_p, int valid, int lane) {
+  const int nz = (BK - valid) * (A_BOXES + B_BOXES);
+  for (int i = lane; i < nz * 8; i += 32) {
+    const int line = i >> 3, chunk = i & 7;
+    const int box = line / (BK - valid), r = valid + line % (BK - valid);
+    uint8_t *base = box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192;
+    *reinterpret_cast<uint4 *>(base + r * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async();
+  __syncwarp();
+}
+
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using TR = ModeTraits<MODE>;
@@ -838,12 +883,34 @@ constexpr int kPairStages = 6;
 constexpr int kPairStageBytes = 32768;
 
 template <int MODE, int BN>
+__device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const SharedState &st, int pt,
+                                                 int rank) {
+  Tile t;
+  if constexpr (ModeTraits<MODE>::red) {
+    const int MT2 = p.M_fixed / 256, NT = p.N / BN;
+    t.g = pt / (MT2 * NT);
+    const int loc = pt % (MT2 * NT);
+    t.n = loc / MT2;
+    t.m = 2 * (loc % MT2) + rank;
+    t.row0 = p.offsets[t.g];
+    t.rows = p.offsets[t.g + 1] - t.row0;
+  } else {
+    t = decode_tile<MODE, BN>(p, st, pt);
+    t.m = 2 * t.m + rank;
+  }
+  return t;
+}
+
+template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
-  static_assert(MODE == GU || MODE == DOWN || MODE == DH || MODE == DX, "row-grouped modes only");
+  static_assert(MODE != RT, "the router GEMM runs single-CTA");
   using TR = ModeTraits<MODE>;
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
   constexpr int HALF_N = MMA_N / 2;
-  constexpr uint32_t kTx = 2u * (kABytes + HALF_N * BK * 2);
+  constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
+  constexpr int B_HALF_BOXES = TR::b_mn ? HALF_N / 64 : 1;
+  constexpr uint32_t kOwnTx = kABytes + HALF_N * BK * 2;   // one CTA's bytes per stage
+  constexpr uint32_t kTx = 2u * kOwnTx;
   constexpr uint32_t kIdesc = instr_desc(256, MMA_N, TR::a_mn, TR::b_mn);
 
   extern __shared__ uint8_t smem_raw[];
@@ -860,16 +927,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     st.abort = 0;
     int total = 0;
     bool bad = false;
-    const int NT = p.N / (MODE == GU ? 128 : BN);
-    for (int g = 0; g < p.n_groups; ++g) {
-      const int rows = p.offsets[g + 1] - p.offsets[g];
-      if (rows < 0) bad = true;
-      const int mt = rows > 0 ? (rows + 255) / 256 : 0;   // 256-row pair tiles
-      st.tile_start[g] = total;
-      st.mtiles[g] = mt > 0 ? mt : 1;
-      total += mt * NT;
+    if constexpr (TR::red) {
+      for (int g = 0; g < p.n_groups; ++g)
+        if (p.offsets[g + 1] < p.offsets[g]) bad = true;
+      total = p.n_groups * (p.M_fixed / 256) * (p.N / BN);   // 256-row pair tiles
+    } else {
+      const int NT = p.N / (MODE == GU ? 128 : BN);
+      for (int g = 0; g < p.n_groups; ++g) {
+        const int rows = p.offsets[g + 1] - p.offsets[g];
+        if (rows < 0) bad = true;
+        const int mt = rows > 0 ? (rows + 255) / 256 : 0;   // 256-row pair tiles
+        st.tile_start[g] = total;
+        st.mtiles[g] = mt > 0 ? mt : 1;
+        total += mt * NT;
+      }
+      st.tile_start[p.n_groups] = total;
     }
-    st.tile_start[p.n_groups] = total;
     if (p.offsets[0] < 0 || (int64_t)p.offsets[p.n_groups] > p.max_rows) bad = true;
     if (bad) {
       report(p.status, MOE_ERR_DEVICE, kInfoOffsets);
@@ -879,6 +952,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     for (int i = 0; i < kPairStages; ++i) {
       mbar_init(smem_u32(&st.full[i]), 1);
       mbar_init(smem_u32(&st.empty[i]), 1);
+      mbar_init(smem_u32(&st.zfull[i]), 1);
+      mbar_init(smem_u32(&st.zready[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&st.tfull[b]), 1);
@@ -910,53 +985,75 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       int last_phase[kPairStages];
 #pragma unroll
       for (int i = 0; i < kPairStages; ++i) last_phase[i] = -1;
+      uint32_t zuse = 0;   // odd CTA: bit s = parity of the next ragged use of stage s
       for (int pt = cid; pt < total && !st.abort; pt += ncl) {
-        Tile t = decode_tile<MODE, BN>(p, st, pt);
-        t.m = 2 * t.m + (int)rank;
-        const int kblocks = p.K_fixed / BK;
+        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
+        const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1;
           if (!wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 1)) break;
-          const uint32_t full_leader = map_to_cta(smem_u32(&st.full[s]), 0);
-          if (leader) mbar_expect_tx(smem_u32(&st.full[s]), kTx);
-          last_phase[s] = (int)ph;
+          const bool ragged = TR::red && (t.rows - kb * BK < BK);
           const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
           const uint32_t sb = sa + kABytes;
-          tma_load_2d_pair(sa, &p.tmA, full_leader, kb * BK, t.row0 + t.m * BM);
-          const int64_t gb = (int64_t)t.g * p.b_group_rows;
-          if constexpr (MODE == GU) {   // even CTA: gate rows, odd CTA: up rows
-            tma_load_2d_pair(sb, &p.tmB, full_leader, kb * BK,
-                             (int)(gb + (int64_t)rank * p.F + t.n * 128));
-          } else if constexpr (TR::b_mn) {
-#pragma unroll
-            for (int b = 0; b < HALF_N / 64; ++b)
-              tma_load_2d_pair(sb + b * 8192, &p.tmB, full_leader,
-                               t.n * BN + (int)rank * HALF_N + 64 * b, (int)(gb + kb * BK));
+          // where this CTA's bytes complete: the even CTA's full barrier, or
+          // for a ragged block of the odd CTA its own zfull barrier (it must
+          // zero its tail rows after they land)
+          uint32_t bar;
+          if (ragged && !leader) {
+            bar = map_to_cta(smem_u32(&st.zfull[s]), rank);
+            mbar_expect_tx(smem_u32(&st.zfull[s]), kOwnTx);
+            zuse ^= 1u << s;
           } else {
-            tma_load_2d_pair(sb, &p.tmB, full_leader, kb * BK,
-                             (int)(gb + t.n * BN + (int)rank * HALF_N));
+            bar = map_to_cta(smem_u32(&st.full[s]), 0);
+            if (leader) mbar_expect_tx(smem_u32(&st.full[s]), ragged ? kOwnTx : kTx);
+          }
+          if (leader) last_phase[s] = (int)ph;
+          if constexpr (TR::red) {
+            const int krow = t.row0 + kb * BK;
+#pragma unroll
+            for (int b = 0; b < A_BOXES; ++b)
+              tma_load_2d_pair(sa + b * 8192, &p.tmA, bar, t.m * BM + 64 * b, krow);
+#pragma unroll
+            for (int b = 0; b < B_HALF_BOXES; ++b)
+              tma_load_2d_pair(sb + b * 8192, &p.tmB, bar, t.n * BN + (int)rank * HALF_N + 64 * b, krow);
+          } else {
+            tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
+            const int64_t gb = (int64_t)t.g * p.b_group_rows;
+            if constexpr (MODE == GU) {   // even CTA: gate rows, odd CTA: up rows
+              tma_load_2d_pair(sb, &p.tmB, bar, kb * BK, (int)(gb + (int64_t)rank * p.F + t.n * 128));
+            } else if constexpr (TR::b_mn) {
+#pragma unroll
+              for (int b = 0; b < B_HALF_BOXES; ++b)
+                tma_load_2d_pair(sb + b * 8192, &p.tmB, bar,
+                                 t.n * BN + (int)rank * HALF_N + 64 * b, (int)(gb + kb * BK));
+            } else {
+              tma_load_2d_pair(sb, &p.tmB, bar, kb * BK, (int)(gb + t.n * BN + (int)rank * HALF_N));
+            }
           }
         }
       }
-      // the even CTA's full barriers see both CTAs' loads land
+      // the even CTA's full barriers see the loads of both CTAs land (the odd
+      // CTA's ragged blocks are seen by its zeroing warp)
       if (leader) {
         for (int i = 0; i < kPairStages; ++i)
           if (last_phase[i] >= 0) {
-            const uint32_t bar = smem_u32(&st.full[i]);
+            const uint32_t b = smem_u32(&st.full[i]);
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(bar, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
+            while (!mbar_try_wait(b, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
             }
           }
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer (even CTA) =======================
     if (leader) {
+      // ======================= MMA issuer (even CTA) =======================
       int it = 0, tcount = 0;
       bool issued_any = false;
+      uint32_t zuse = 0;   // bit s = parity of the next ragged use of stage s
       for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
-        const int kblocks = p.K_fixed / BK;
+        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, 0);
+        const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
         const int buf = tcount & 1;
         const uint32_t use = (tcount >> 1) & 1;
         if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2))) break;
@@ -970,14 +1067,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
             ok = false;
             break;
           }
+          if constexpr (TR::red) {
+            const int valid = t.rows - kb * BK;
+            if (valid < BK) {
+              zero_tail_rows<A_BOXES, B_HALF_BOXES>(smem + s * kPairStageBytes, valid, lane);
+              const uint32_t zp = (zuse >> s) & 1;
+              zuse ^= 1u << s;
+              if (!__all_sync(0xffffffffu, wait_bounded_cluster(st, smem_u32(&st.zready[s]), zp, p.status, 6))) {
+                ok = false;
+                break;
+              }
+            }
+          }
           tc_fence_after();
           if (lane == 0) {
             const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
             const uint32_t sb = sa + kABytes;
 #pragma unroll
             for (int ks = 0; ks < BK / 16; ++ks) {
-              const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
-              uint64_t bd;
+              uint64_t ad, bd;
+              if constexpr (TR::a_mn) ad = smem_desc(sa + ks * 2048, 8192, 1024);
+              else ad = smem_desc(sa + ks * 32, 16, 1024);
               if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
               else bd = smem_desc(sb + ks * 32, 16, 1024);
               tc_mma_pair(dcol, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
@@ -999,6 +1109,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         }
       }
       __syncwarp();
+    } else if constexpr (TR::red) {
+      // ============ odd CTA: zero the tail rows of its ragged blocks ============
+      int it = 0;
+      uint32_t zuse = 0;
+      const uint32_t zready_leader0 = map_to_cta(smem_u32(&st.zready[0]), 0);
+      for (int pt = cid; pt < total && !st.abort; pt += ncl) {
+        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, 1);
+        const int kblocks = (t.rows + BK - 1) / BK;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int valid = t.rows - kb * BK;
+          if (valid >= BK) continue;
+          const int s = it % kPairStages;
+          const uint32_t zp = (zuse >> s) & 1;
+          zuse ^= 1u << s;
+          if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.zfull[s]), zp, p.status, 7))) break;
+          zero_tail_rows<A_BOXES, B_HALF_BOXES>(smem + s * kPairStageBytes, valid, lane);
+          if (lane == 0) mbar_arrive_cluster(zready_leader0 + s * 8);
+          __syncwarp();
+        }
+      }
     }
   } else {
     // ======================= epilogue (both CTAs) =======================
@@ -1007,8 +1137,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     uint32_t ephase = 0;
     int tcount = 0;
     for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
-      Tile t = decode_tile<MODE, BN>(p, st, pt);
-      t.m = 2 * t.m + (int)rank;
+      const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
       const int buf = tcount & 1;
       const uint32_t use = (tcount >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
@@ -1140,8 +1269,10 @@ bool pair_enabled() {
 template <int MODE>
 cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
   const bool bn256 = !(MODE == GU || p.N % 256 != 0);
-  if constexpr (MODE == GU || MODE == DOWN || MODE == DH || MODE == DX) {
-    if (pair_enabled()) return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
+  if constexpr (MODE != RT) {
+    const bool red = (MODE == WGD || MODE == WGU);
+    if (pair_enabled() && (!red || p.M_fixed % 256 == 0))
+      return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
   }
   return bn256 ? launch_mode<MODE, 256>(p, s) : launch_mode<MODE, 128>(p, s);
 }
