@@ -78,6 +78,7 @@ struct TcParams {
   void *out0;    // GU: H; DOWN: Yp; DH: dA; DX: dXp; WG*: dW
   void *out1;    // GU: A_save (nullable)
   const void *aux;  // DH: A_save
+  int fault_stall;   // test hook: the producer issues no loads (waits run out)
   // RT
   int64_t T;
   int E, e_pad, has_gate;
@@ -710,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   if (warp == 0) {
     // ======================= TMA producer =======================
-    if (lane == 0) {
+    if (lane == 0 && !p.fault_stall) {
       int it = 0;
       int last_phase[kStages];
 #pragma unroll
@@ -980,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 
   if (warp == 0) {
     // ======================= TMA producer (both CTAs) =======================
-    if (lane == 0) {
+    if (lane == 0 && !p.fault_stall) {
       int it = 0;
       int last_phase[kPairStages];
 #pragma unroll
@@ -1223,8 +1224,17 @@ int num_sms() {
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
 
+// Fault injection for tests of the timeout path: with MOE_FAULT_INJECT_STALL=1
+// the producer warp issues no loads, so the MMA warp's first wait runs out;
+// the kernel then records MOE_ERR_TIMEOUT and returns.
+int fault_stall() {
+  const char *e = getenv("MOE_FAULT_INJECT_STALL");
+  return (e != nullptr && e[0] == '1') ? 1 : 0;
+}
+
 template <int MODE, int BN>
-cudaError_t launch_mode(const TcParams &p, cudaStream_t s) {
+cudaError_t launch_mode(TcParams p, cudaStream_t s) {
+  p.fault_stall = fault_stall();
   auto k = tc_gemm_kernel<MODE, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -1236,7 +1246,8 @@ constexpr size_t kPairSmemBytes =
     kPairStages * kPairStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
 
 template <int MODE, int BN>
-cudaError_t launch_pair(const TcParams &p, cudaStream_t s) {
+cudaError_t launch_pair(TcParams p, cudaStream_t s) {
+  p.fault_stall = fault_stall();
   auto k = tc_gemm_pair_kernel<MODE, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
   if (e != cudaSuccess) return e;

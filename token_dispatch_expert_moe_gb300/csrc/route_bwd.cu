@@ -8,10 +8,9 @@
 //      arithmetic as the forward); dp on the Top-K slots
 //      ((g - <g,w>) / Z with renorm, g without); dl = p (dp - <p,dp>).
 //   2. dx_kernel: dx_router[t] = dx_in[t] + sum_e dl[t,e] W_r[e] + dz[t] w_sg,
-//      64 tokens x 256 hidden columns per CTA, each thread's W_r column in
-//      registers.
-//   3. wgrad_partial_kernel: per chunk of tokens, partial sums of
-//      dl^T x (and dz^T x), then reduce_kernel adds the chunks in order:
+//      register-tiled (4 tokens x 4 columns per thread);
+//   3. wgrad_partial_kernel: per chunk of tokens, partial sums of dl^T x (and
+//      dz^T x), register-tiled; reduce_kernel adds the chunks in order:
 //      deterministic, no atomics.
 #include "common.cuh"
 #include "softmax.cuh"
@@ -19,8 +18,7 @@
 namespace moe {
 namespace {
 
-constexpr int kDxTok = 64;   // tokens per dx CTA
-constexpr int kCols = 256;   // hidden columns per CTA
+constexpr int kCols = 256;   // hidden columns per dW_r CTA
 constexpr int kChunks = 32;  // token chunks of the dW_r partial sums
 
 __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
@@ -53,75 +51,90 @@ __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
 }
 
 // dx_router[t, j] = dx_in[t, j] + sum_c dl[t, c] W[c, j]  (row c = E is w_sg
-// with dl = dz). One thread per column j holds W[:, j] in registers for 64
-// tokens; dl rows are read from shared memory as float4 broadcasts.
+// with dl = dz). A 64-token x 64-column tile per CTA with both operands in
+// shared memory (dl transposed, W converted to fp32); each thread computes 4
+// tokens x 4 columns, so one float4 of dl and one of W feed 16 FMAs. The sum
+// over c runs in a fixed order per output.
+constexpr int kDxT = 64, kDxJ = 64;
 template <typename T, int CP>
-__global__ void __launch_bounds__(kCols) dx_kernel(RouteBwdArgs a) {
-  __shared__ __align__(16) float dls[kDxTok][CP];
+__global__ void __launch_bounds__(256) dx_kernel(RouteBwdArgs a) {
+  __shared__ __align__(16) float dlT[CP][kDxT];
+  __shared__ __align__(16) float Ws[CP][kDxJ];
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
-  const int64_t t0 = (int64_t)blockIdx.x * kDxTok;
-  const int j = blockIdx.y * kCols + threadIdx.x;
+  const int64_t t0 = (int64_t)blockIdx.x * kDxT;
+  const int j0 = blockIdx.y * kDxJ;
   const T *W = reinterpret_cast<const T *>(a.W_r);
   const T *wsg = reinterpret_cast<const T *>(a.w_sg);
-  float w[CP];
-#pragma unroll
-  for (int c = 0; c < CP; ++c)
-    w[c] = (j < a.d && c < C) ? to_f32(c < E ? W[(int64_t)c * a.d + j] : wsg[j]) : 0.0f;
-  for (int i = threadIdx.x; i < kDxTok * CP; i += blockDim.x) {
+  for (int i = threadIdx.x; i < CP * kDxJ; i += blockDim.x) {
+    const int c = i / kDxJ, jj = i % kDxJ, j = j0 + jj;
+    float v = 0.0f;
+    if (c < C && j < a.d) v = to_f32(c < E ? W[(int64_t)c * a.d + j] : wsg[j]);
+    Ws[c][jj] = v;
+  }
+  for (int i = threadIdx.x; i < CP * kDxT; i += blockDim.x) {
     const int tt = i / CP, c = i % CP;
     const int64_t t = t0 + tt;
     float v = 0.0f;
     if (t < a.T && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
-    dls[tt][c] = v;
+    dlT[c][tt] = v;
   }
   __syncthreads();
-  if (j >= a.d) return;
-  // two tokens at a time, four partial sums each (combined in a fixed order)
-  for (int tt = 0; tt < kDxTok; tt += 2) {
-    const int64_t t = t0 + tt;
-    if (t >= a.T) break;
-    const bool two = t + 1 < a.T;
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+  const int tq = threadIdx.x >> 4;   // token quad 0..15
+  const int jq = threadIdx.x & 15;   // column quad 0..15
+  float acc[4][4];
 #pragma unroll
-    for (int c = 0; c < CP; c += 4) {
-      const float4 v = *reinterpret_cast<const float4 *>(&dls[tt][c]);
-      const float4 u = *reinterpret_cast<const float4 *>(&dls[tt + 1][c]);
-      p0[0] = fmaf(v.x, w[c], p0[0]);
-      p0[1] = fmaf(v.y, w[c + 1], p0[1]);
-      p0[2] = fmaf(v.z, w[c + 2], p0[2]);
-      p0[3] = fmaf(v.w, w[c + 3], p0[3]);
-      p1[0] = fmaf(u.x, w[c], p1[0]);
-      p1[1] = fmaf(u.y, w[c + 1], p1[1]);
-      p1[2] = fmaf(u.z, w[c + 2], p1[2]);
-      p1[3] = fmaf(u.w, w[c + 3], p1[3]);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[i][k] = 0.0f;
+#pragma unroll 4
+  for (int c = 0; c < CP; ++c) {
+    const float4 dv = *reinterpret_cast<const float4 *>(&dlT[c][tq * 4]);
+    const float4 wv = *reinterpret_cast<const float4 *>(&Ws[c][jq * 4]);
+    const float d4[4] = {dv.x, dv.y, dv.z, dv.w};
+    const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(d4[i], w4[k], acc[i][k]);
+  }
+  const int j = j0 + jq * 4;
+  if (j >= a.d) return;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = t0 + tq * 4 + i;
+    if (t >= a.T) break;
+    float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    if (a.dx_in != nullptr) {
+      const float4 xi = *reinterpret_cast<const float4 *>(a.dx_in + t * a.d + j);
+      o.x += xi.x; o.y += xi.y; o.z += xi.z; o.w += xi.w;
     }
-    const float in0 = a.dx_in != nullptr ? a.dx_in[t * a.d + j] : 0.0f;
-    a.dx_router[t * a.d + j] = in0 + ((p0[0] + p0[1]) + (p0[2] + p0[3]));
-    if (two) {
-      const float in1 = a.dx_in != nullptr ? a.dx_in[(t + 1) * a.d + j] : 0.0f;
-      a.dx_router[(t + 1) * a.d + j] = in1 + ((p1[0] + p1[1]) + (p1[2] + p1[3]));
-    }
+    *reinterpret_cast<float4 *>(a.dx_router + t * a.d + j) = o;
   }
 }
 
-// Partial sums over one chunk of tokens of dl^T x (and dz^T x): one thread per
-// column j keeps CP accumulators; 32 tokens of dl and x are staged in shared
-// memory per step.
+// Partial sums over one chunk of tokens of dl^T x (row E: dz^T x): a
+// CP x 256 tile per CTA (CP a multiple of 8, rows >= C zero), each thread
+// CP/8 rows x 8 columns. Per token a thread reads CP/8 dl values and one
+// 16-byte x vector from shared memory for CP FMAs.
 template <typename T, int CP>
-__global__ void __launch_bounds__(kCols) wgrad_partial_kernel(RouteBwdArgs a, int64_t chunk) {
+__global__ void __launch_bounds__(256) wgrad_partial_kernel(RouteBwdArgs a, int64_t chunk) {
+  constexpr int RPT = CP / 8;   // rows of the tile per thread
   __shared__ __align__(16) float dls[32][CP];
-  __shared__ float xs[32][kCols];
+  __shared__ __align__(16) float xs[32][kCols];
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
   const int64_t tb = (int64_t)blockIdx.x * chunk;
   const int64_t te = min(a.T, tb + chunk);
   const int j0 = blockIdx.y * kCols;
-  const int j = j0 + threadIdx.x;
+  const int rg = threadIdx.x >> 5;   // row group 0..7 (one per warp)
+  const int jo = threadIdx.x & 31;   // column octet 0..31
   const T *x = reinterpret_cast<const T *>(a.x);
-  float acc[CP];
+  float acc[RPT][8];
 #pragma unroll
-  for (int c = 0; c < CP; ++c) acc[c] = 0.0f;
+  for (int r = 0; r < RPT; ++r)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[r][k] = 0.0f;
   for (int64_t s0 = tb; s0 < te; s0 += 32) {
     __syncthreads();
     for (int i = threadIdx.x; i < 32 * CP; i += blockDim.x) {
@@ -131,30 +144,43 @@ __global__ void __launch_bounds__(kCols) wgrad_partial_kernel(RouteBwdArgs a, in
       if (t < te && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
       dls[tt][c] = v;
     }
-#pragma unroll 8
-    for (int tt = 0; tt < 32; ++tt) {
+    for (int i = threadIdx.x; i < 32 * kCols; i += blockDim.x) {
+      const int tt = i / kCols, jj = i % kCols;
       const int64_t t = s0 + tt;
-      xs[tt][threadIdx.x] = (t < te && j < a.d) ? to_f32(x[t * a.d + j]) : 0.0f;
+      xs[tt][jj] = (t < te && j0 + jj < a.d) ? to_f32(x[t * a.d + j0 + jj]) : 0.0f;
     }
     __syncthreads();
     const int n = (int)min((int64_t)32, te - s0);
     for (int tt = 0; tt < n; ++tt) {
-      const float xv = xs[tt][threadIdx.x];
+      const float4 x0 = *reinterpret_cast<const float4 *>(&xs[tt][jo * 8]);
+      const float4 x1 = *reinterpret_cast<const float4 *>(&xs[tt][jo * 8 + 4]);
+      const float x8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-      for (int c = 0; c < CP; c += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(&dls[tt][c]);
-        acc[c] = fmaf(v.x, xv, acc[c]);
-        acc[c + 1] = fmaf(v.y, xv, acc[c + 1]);
-        acc[c + 2] = fmaf(v.z, xv, acc[c + 2]);
-        acc[c + 3] = fmaf(v.w, xv, acc[c + 3]);
+      for (int r = 0; r < RPT; ++r) {
+        const float dv = dls[tt][rg * RPT + r];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[r][k] = fmaf(dv, x8[k], acc[r][k]);
       }
     }
   }
+  const int j = j0 + jo * 8;
   if (j >= a.d) return;
   float *part = a.partial + (int64_t)blockIdx.x * C * a.d;
 #pragma unroll
-  for (int c = 0; c < CP; ++c)
-    if (c < C) part[(int64_t)c * a.d + j] = acc[c];
+  for (int r = 0; r < RPT; ++r) {
+    const int c = rg * RPT + r;
+    if (c < C) {
+      float *dst = part + (int64_t)c * a.d + j;
+      if (j + 8 <= a.d) {
+        *reinterpret_cast<float4 *>(dst) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+        *reinterpret_cast<float4 *>(dst + 4) = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (j + k < a.d) dst[k] = acc[r][k];
+      }
+    }
+  }
 }
 
 __global__ void reduce_kernel(RouteBwdArgs a, int nchunk) {
@@ -189,7 +215,7 @@ size_t route_bwd_workspace_bytes(int64_t T, int d, int E) {
 
 template <int CP>
 void launch_cp(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk) {
-  dim3 gdx((unsigned)((a.T + kDxTok - 1) / kDxTok), (unsigned)((a.d + kCols - 1) / kCols));
+  dim3 gdx((unsigned)((a.T + kDxT - 1) / kDxT), (unsigned)((a.d + kDxJ - 1) / kDxJ));
   dim3 gw((unsigned)nchunk, (unsigned)((a.d + kCols - 1) / kCols));
   if (a.dtype == MOE_BF16) {
     dx_kernel<__nv_bfloat16, CP><<<gdx, kCols, 0, s>>>(a);
@@ -208,7 +234,7 @@ cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
   if (C <= 8) launch_cp<8>(a, s, chunk, nchunk);
   else if (C <= 16) launch_cp<16>(a, s, chunk, nchunk);
   else if (C <= 32) launch_cp<32>(a, s, chunk, nchunk);
-  else launch_cp<68>(a, s, chunk, nchunk);
+  else launch_cp<72>(a, s, chunk, nchunk);
   const int64_t n = (int64_t)C * a.d;
   reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, nchunk);
   if (a.db_r != nullptr) db_kernel<<<a.E, 1024, 0, s>>>(a);
