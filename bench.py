@@ -173,7 +173,7 @@ def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = Non
 def launches_per_step(cfg) -> int:
     n = (2 if cfg.dtype == "bf16" else 1)  # router: logits GEMM + Top-K (fp32: one fused kernel)
     n += 1 if cfg.drop else 0             # capacity
-    n += 4                                 # map count, scan, scatter, row copy
+    n += 3                                 # map count, map scatter, row copy
     n += 2 + (2 if cfg.Fs else 0)          # grouped GEMMs (routed [+ shared])
     n += 1                                 # un-permute
     if cfg.backward:

@@ -52,7 +52,7 @@ def test_aggregate_single_rank():
 def test_launch_counts():
     import bench
     from synthetic import get_config
-    assert bench.launches_per_step(get_config("mixtral_8x22b")) == 10
-    assert bench.launches_per_step(get_config("llama3_8x70b")) == 9 + 10
-    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 11 + 15
-    assert bench.launches_per_step(get_config("tiny_f32")) == 8
+    assert bench.launches_per_step(get_config("mixtral_8x22b")) == 9
+    assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 10
+    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 15
+    assert bench.launches_per_step(get_config("tiny_f32")) == 7

@@ -11,11 +11,12 @@
 //   1. map_count: tokens are cut into blocks of 256; each CTA sets one bit per
 //      kept (token, expert) in a shared bitmap [E][8 words] and writes the
 //      per-expert popcounts of its block;
-//   2. map_scan: per expert, an exclusive scan over blocks; counts, offsets;
-//   3. map_scatter: each CTA rebuilds its bitmap; the rank of token t among
+//   2. map_scatter: each CTA reads the per-block counts, forms the expert
+//      totals and offsets (CTA 0 publishes counts and offsets) and its own
+//      base per expert; it rebuilds its bitmap, and the rank of token t among
 //      the kept tokens of expert e in the block is the popcount of the bits
-//      below t, so row_of[t,k] = base[block][e] + rank, and src_of[row] =
-//      t*K + k. Rows come out expert-major and token-ascending.
+//      below t, so row_of[t,k] = base[e] + rank, and src_of[row] = t*K + k.
+//      Rows come out expert-major and token-ascending.
 #include <mutex>
 
 #include "common.cuh"
@@ -52,42 +53,36 @@ __global__ void __launch_bounds__(kMapBlock) map_count_kernel(PermuteArgs a) {
   }
 }
 
-// One CTA: thread e scans expert e's block counts (in block order).
-__global__ void map_scan_kernel(PermuteArgs a, int nblk) {
-  __shared__ int tot[64];
-  const int E = a.E;
-  const int e = threadIdx.x;
-  if (e < E) {
-    int run = 0;
-    for (int b = 0; b < nblk; ++b) {
-      const int c = a.blk_counts[(int64_t)b * E + e];
-      a.blk_counts[(int64_t)b * E + e] = run;  // exclusive prefix within expert
-      run += c;
-    }
-    tot[e] = run;
-    a.counts[e] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int i = 0; i < E; ++i) {
-      a.offsets[i] = acc;
-      acc += tot[i];
-    }
-    a.offsets[E] = acc;
-  }
-  __syncthreads();
-  if (e < E) {
-    int base = 0;
-    for (int i = 0; i < e; ++i) base += tot[i];
-    for (int b = 0; b < nblk; ++b) a.blk_counts[(int64_t)b * E + e] += base;
-  }
-}
-
-__global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a) {
+__global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a, int nblk) {
   extern __shared__ uint32_t bm[];  // [E][8]
+  __shared__ int tot_s[64], base_s[64];
   const int E = a.E, K = a.K;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0;
+  // every CTA scans the (small) table of per-block counts itself: expert
+  // totals, and the kept assignments of expert e in blocks before this one
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int tot = 0, before = 0;
+    for (int b = 0; b < nblk; ++b) {
+      const int c = a.blk_counts[(int64_t)b * E + e];
+      before += b < (int)blockIdx.x ? c : 0;
+      tot += c;
+    }
+    tot_s[e] = tot;
+    base_s[e] = before;
+  }
+  __syncthreads();
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int off = 0;
+    for (int i = 0; i < e; ++i) off += tot_s[i];
+    base_s[e] += off;
+    if (blockIdx.x == 0) {
+      a.counts[e] = tot_s[e];
+      a.offsets[e] = off;
+      if (e == E - 1) a.offsets[E] = off + tot_s[e];
+    }
+  }
   __syncthreads();
   const int64_t t = (int64_t)blockIdx.x * kMapBlock + threadIdx.x;
   const int wi = threadIdx.x >> 5;
@@ -106,7 +101,7 @@ __global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a) {
       if (a.keep[t * K + k] && e >= 0 && e < E) {
         int rank = __popc(bm[e * 8 + wi] & below);
         for (int w = 0; w < wi; ++w) rank += __popc(bm[e * 8 + w]);
-        row = a.blk_counts[(int64_t)blockIdx.x * E + e] + rank;
+        row = base_s[e] + rank;
         a.src_of[row] = (int32_t)(t * K + k);
       }
       a.row_of[t * K + k] = row;
@@ -114,27 +109,68 @@ __global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a) {
   }
 }
 
-// Xp[row_of[t,k]] = x[t]: one CTA per token, 16-byte vectors; x is read
-// once and written to each kept slot's row.
-template <typename T>
-__global__ void __launch_bounds__(256) permute_rows_kernel(PermuteArgs a) {
-  const int64_t t = blockIdx.x;
-  const int K = a.K;
-  __shared__ int32_t rows[8];
-  if (threadIdx.x < K) rows[threadIdx.x] = a.row_of[t * K + threadIdx.x];
-  __syncthreads();
-  const int nv = a.d / Vec<T>::N;
-  const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.x) + t * a.d);
-  uint4 *dst = reinterpret_cast<uint4 *>(a.Xp);
-  const int64_t row_vecs = nv;
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
-    const uint4 val = src[v];
-#pragma unroll 8
-    for (int k = 0; k < K; ++k) {
-      const int32_t r = rows[k];
-      if (r >= 0) dst[(int64_t)r * row_vecs + v] = val;
+// Xp[row_of[t,k]] = x[t] with the bulk-copy engine: a one-warp CTA loads up
+// to 4 token rows (at most 96 KB) into shared memory (cp.async.bulk, one
+// mbarrier), then writes each row to its kept slots' rows with bulk stores.
+// x is read once; the SM issues a handful of instructions per row.
+constexpr int kPermTokens = 4;
+constexpr uint32_t kPermSmemCap = 96 * 1024;
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__global__ void __launch_bounds__(32) permute_bulk_kernel(PermuteArgs a, uint32_t row_bytes,
+                                                          int tpc) {
+  extern __shared__ __align__(128) uint8_t rows_smem[];
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const int64_t t0 = (int64_t)blockIdx.x * tpc;
+  const int n = (int)min((int64_t)tpc, a.T - t0);
+  const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  const uint32_t sm = static_cast<uint32_t>(__cvta_generic_to_shared(rows_smem));
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
+               "r"(row_bytes * (uint32_t)n)
+               : "memory");
+  const uint8_t *x = static_cast<const uint8_t *>(a.x);
+  for (int i = 0; i < n; ++i)
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            sm + i * row_bytes),
+        "l"(x + (t0 + i) * (int64_t)row_bytes), "r"(row_bytes), "r"(b)
+        : "memory");
+  // bounded wait for the rows to land
+  uint32_t done = 0;
+  const uint64_t start = now_ns();
+  while (!done) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(b)
+        : "memory");
+    if (!done && now_ns() - start > 2000000000ull) {
+      report(a.status, MOE_ERR_TIMEOUT, kInfoRowRange);
+      return;
     }
   }
+  uint8_t *Xp = static_cast<uint8_t *>(a.Xp);
+  for (int i = 0; i < n; ++i) {
+    for (int k = 0; k < a.K; ++k) {
+      const int32_t r = a.row_of[(t0 + i) * a.K + k];
+      if (r >= 0)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                         Xp + (int64_t)r * row_bytes),
+                     "r"(sm + i * row_bytes), "r"(row_bytes)
+                     : "memory");
+    }
+  }
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // out[t] = sum_k w[t,k] Yp[row_of[t,k]] (+ sigmoid(z_t) Ys[t]), fp32 sum in
@@ -272,8 +308,8 @@ permute_bwd_kernel(int64_t T, int d, int K, const float *__restrict__ dXp,
 // build live in this fixed device array instead of a caller workspace. It
 // holds MOE_PERMUTE_NOALLOC_MAX_TOKENS / 256 blocks x 64 experts (128 KB) and
 // stays resident on every GPU that loads the library until the process exits.
-// map_count writes every word that map_scan and map_scatter later read, so a
-// call never sees the previous call's counts and nothing needs clearing.
+// map_count writes every word that map_scatter later reads, so a call never
+// sees the previous call's counts and nothing needs clearing.
 constexpr int kNoAllocBlocks = MOE_PERMUTE_NOALLOC_MAX_TOKENS / kMapBlock;
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocBlocks * 64];
 
@@ -316,12 +352,16 @@ cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   const int nblk = (int)((a.T + kMapBlock - 1) / kMapBlock);
   const size_t bm_bytes = (size_t)a.E * 8 * sizeof(uint32_t);
   map_count_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a);
-  map_scan_kernel<<<1, 64, 0, s>>>(a, nblk);
-  map_scatter_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a);
-  if (a.dtype == MOE_BF16)
-    permute_rows_kernel<__nv_bfloat16><<<(unsigned)a.T, 256, 0, s>>>(a);
-  else
-    permute_rows_kernel<float><<<(unsigned)a.T, 256, 0, s>>>(a);
+  map_scatter_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a, nblk);
+  const uint32_t row_bytes = (uint32_t)a.d * (a.dtype == MOE_BF16 ? 2u : 4u);
+  int tpc = kPermTokens;
+  while (tpc > 1 && (uint32_t)tpc * row_bytes > kPermSmemCap) --tpc;
+  const size_t smem = (size_t)tpc * row_bytes;
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;  // rows wider than the bulk path holds
+  cudaError_t e = cudaFuncSetAttribute(permute_bulk_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  permute_bulk_kernel<<<(unsigned)((a.T + tpc - 1) / tpc), 32, smem, s>>>(a, row_bytes, tpc);
   return cudaGetLastError();
 }
 
