@@ -112,9 +112,11 @@ __global__ void __launch_bounds__(256) topk_from_logits_kernel(RouteArgs a) {
 // probability, then a lower token index. Keys are unique, so the cap largest
 // are found exactly by an 8-pass MSB radix select of the cap-th largest key.
 constexpr int kCapThreads = 512;
+constexpr int kCapSmemKeys = 16384;   // candidates kept in shared memory (128 KB)
 
 __global__ void __launch_bounds__(kCapThreads)
-capacity_kernel(RouteArgs a, int cap_full, int cap_last) {
+capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
+  extern __shared__ unsigned long long skeys[];
   __shared__ uint32_t n_cand;
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long sh_prefix;
@@ -123,8 +125,10 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last) {
   const int64_t lo = (int64_t)j * a.S;
   const int64_t hi = min(a.T, lo + a.S);
   const int cap = (hi - lo == a.S) ? cap_full : cap_last;
-  unsigned long long *keys = a.cap_keys + ((int64_t)j * a.E + e) * a.S;
+  unsigned long long *keys =
+      keys_in_smem ? skeys : a.cap_keys + ((int64_t)j * a.E + e) * a.S;
   const int K = a.K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) n_cand = 0;
   __syncthreads();
   for (int64_t t = lo + threadIdx.x; t < hi; t += blockDim.x) {
@@ -151,15 +155,35 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last) {
         if ((key & hmask) == (pre & hmask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        uint32_t need = sh_need, cum = 0;
-        int digit = 0;
-        for (int b = 255; b >= 0; --b) {
-          if (cum + hist[b] >= need) { digit = b; need -= cum; break; }
-          cum += hist[b];
+      if (warp == 0) {
+        // digit holding the need-th largest key: lane l owns bins 255-8l down
+        // to 248-8l; an inclusive scan over lanes counts the keys above
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hist[255 - 8 * lane - i];
+          sum += c[i];
         }
-        sh_need = need;
-        sh_prefix = pre | ((unsigned long long)digit << shift);
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const uint32_t excl = incl - sum;
+        const uint32_t need = sh_need;
+        const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+        if (lane == __ffs(hit) - 1) {
+          uint32_t cum = excl;
+          int digit = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (cum + c[i] >= need) { digit = 255 - 8 * lane - i; break; }
+            cum += c[i];
+          }
+          sh_need = need - cum;
+          sh_prefix = pre | ((unsigned long long)digit << shift);
+        }
       }
       __syncthreads();
     }
@@ -212,7 +236,12 @@ cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s) {
   const int cap_full = capacity_of(a.cf, a.S, a.K, a.E);
   const int cap_last = capacity_of(a.cf, last, a.K, a.E);
   dim3 grid((unsigned)n_sub, (unsigned)a.E);
-  capacity_kernel<<<grid, kCapThreads, 0, s>>>(a, cap_full, cap_last);
+  const int in_smem = a.S <= kCapSmemKeys ? 1 : 0;
+  const size_t smem = in_smem ? (size_t)a.S * sizeof(unsigned long long) : 0;
+  cudaError_t e = cudaFuncSetAttribute(capacity_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  capacity_kernel<<<grid, kCapThreads, smem, s>>>(a, cap_full, cap_last, in_smem);
   return cudaGetLastError();
 }
 
