@@ -52,6 +52,7 @@ constexpr int kStages = 4;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr int kPairThreads = 224;  // + warp 6: zeroes ragged K blocks (weight-gradient modes)
 constexpr int kABytes = BM * BK * 2;          // 16 KB
 constexpr int kBBytesMax = 256 * BK * 2;      // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
@@ -309,8 +310,9 @@ struct SharedState {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t ebar[4];  // DH: per-epilogue-warp A_save box loads
-  uint64_t zfull[kMaxStages];   // pair WG*: odd CTA's own ragged-block loads
+  uint64_t zfull[kMaxStages];   // pair WG*: this CTA's own ragged-block loads
   uint64_t zready[kMaxStages];  // pair WG*: odd CTA has zeroed its tail rows
+  uint64_t zdone[kMaxStages];   // pair WG*: even CTA's zeroing warp is done
   uint32_t tmem_base;
   volatile int abort;
   int total_tiles;
@@ -903,7 +905,7 @@ __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const Shared
 }
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
   using TR = ModeTraits<MODE>;
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
@@ -955,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       mbar_init(smem_u32(&st.empty[i]), 1);
       mbar_init(smem_u32(&st.zfull[i]), 1);
       mbar_init(smem_u32(&st.zready[i]), 1);
+      mbar_init(smem_u32(&st.zdone[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&st.tfull[b]), 1);
@@ -986,7 +989,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       int last_phase[kPairStages];
 #pragma unroll
       for (int i = 0; i < kPairStages; ++i) last_phase[i] = -1;
-      uint32_t zuse = 0;   // odd CTA: bit s = parity of the next ragged use of stage s
+      uint32_t zuse = 0;    // bit s = parity of the next ragged use of stage s
+      uint32_t zlast = 0;   // bit s: stage s had a ragged use
       for (int pt = cid; pt < total && !st.abort; pt += ncl) {
         const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
         const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
@@ -998,16 +1002,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
           const uint32_t sb = sa + kABytes;
           // where this CTA's bytes complete: the even CTA's full barrier, or
-          // for a ragged block of the odd CTA its own zfull barrier (it must
-          // zero its tail rows after they land)
+          // for a ragged block this CTA's own zfull barrier (its zeroing warp
+          // clears the tail rows after they land). full[s] still completes
+          // once per use of the stage: for a ragged block by a plain arrival.
           uint32_t bar;
-          if (ragged && !leader) {
+          if (ragged) {
             bar = map_to_cta(smem_u32(&st.zfull[s]), rank);
             mbar_expect_tx(smem_u32(&st.zfull[s]), kOwnTx);
             zuse ^= 1u << s;
+            zlast |= 1u << s;
+            if (leader) mbar_arrive(smem_u32(&st.full[s]));
           } else {
             bar = map_to_cta(smem_u32(&st.full[s]), 0);
-            if (leader) mbar_expect_tx(smem_u32(&st.full[s]), ragged ? kOwnTx : kTx);
+            if (leader) mbar_expect_tx(smem_u32(&st.full[s]), kTx);
           }
           if (leader) last_phase[s] = (int)ph;
           if constexpr (TR::red) {
@@ -1034,16 +1041,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           }
         }
       }
-      // the even CTA's full barriers see the loads of both CTAs land (the odd
-      // CTA's ragged blocks are seen by its zeroing warp)
-      if (leader) {
-        for (int i = 0; i < kPairStages; ++i)
-          if (last_phase[i] >= 0) {
-            const uint32_t b = smem_u32(&st.full[i]);
-            const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(b, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
-            }
+      // wait (bounded) for this CTA's copies still in flight: the even CTA's
+      // full barriers see the loads of both CTAs land; each CTA's zfull
+      // barriers see its own ragged blocks land
+      for (int i = 0; i < kPairStages; ++i) {
+        if (leader && last_phase[i] >= 0) {
+          const uint32_t b = smem_u32(&st.full[i]);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(b, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
           }
+        }
+        if ((zlast >> i) & 1) {
+          const uint32_t b = smem_u32(&st.zfull[i]);
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(b, ((zuse >> i) & 1) ^ 1) && globaltimer() - t0 < kTimeoutNs) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -1070,11 +1083,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           }
           if constexpr (TR::red) {
             const int valid = t.rows - kb * BK;
-            if (valid < BK) {
-              zero_tail_rows<A_BOXES, B_HALF_BOXES>(smem + s * kPairStageBytes, valid, lane);
+            if (valid < BK) {   // both CTAs' zeroing warps have cleared the tail rows
               const uint32_t zp = (zuse >> s) & 1;
               zuse ^= 1u << s;
-              if (!__all_sync(0xffffffffu, wait_bounded_cluster(st, smem_u32(&st.zready[s]), zp, p.status, 6))) {
+              if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.zdone[s]), zp, p.status, 8)) ||
+                  !__all_sync(0xffffffffu, wait_bounded_cluster(st, smem_u32(&st.zready[s]), zp, p.status, 6))) {
                 ok = false;
                 break;
               }
@@ -1110,13 +1123,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         }
       }
       __syncwarp();
-    } else if constexpr (TR::red) {
-      // ============ odd CTA: zero the tail rows of its ragged blocks ============
+    }
+  } else if (warp == 6) {
+    // ===== both CTAs (weight-gradient modes): zero ragged K blocks' tail rows =====
+    // A ragged block's loads complete on this CTA's zfull[s], whose phases
+    // count the ragged uses of stage s only, so this warp waits for each of
+    // them in order. After zeroing: the even CTA signals its MMA warp through
+    // zdone[s], the odd CTA arrives on the even CTA's zready[s] (release,
+    // cluster scope).
+    if constexpr (TR::red) {
       int it = 0;
       uint32_t zuse = 0;
       const uint32_t zready_leader0 = map_to_cta(smem_u32(&st.zready[0]), 0);
       for (int pt = cid; pt < total && !st.abort; pt += ncl) {
-        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, 1);
+        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
         const int kblocks = (t.rows + BK - 1) / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int valid = t.rows - kb * BK;
@@ -1126,7 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           zuse ^= 1u << s;
           if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.zfull[s]), zp, p.status, 7))) break;
           zero_tail_rows<A_BOXES, B_HALF_BOXES>(smem + s * kPairStageBytes, valid, lane);
-          if (lane == 0) mbar_arrive_cluster(zready_leader0 + s * 8);
+          if (lane == 0) {
+            if (leader) mbar_arrive(smem_u32(&st.zdone[s]));
+            else mbar_arrive_cluster(zready_leader0 + s * 8);
+          }
           __syncwarp();
         }
       }
@@ -1253,7 +1276,7 @@ cudaError_t launch_pair(TcParams p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPairThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
