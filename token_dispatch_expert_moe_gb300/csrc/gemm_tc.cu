@@ -411,9 +411,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
       stage_row(b, lane, w);
       stage_store(b, &p.tmO0, t.n * BN + c * 32, y, lane);
     }
-  } else if (t.rows - t.m * BM >= BM) {
-    // whole tile of one group: bulk stores (rows past the group would
-    // belong to the next group, so partial tiles take the path below)
+  } else if (t.rows - t.m * BM - q * 32 >= 32) {
+    // this warp's 32 rows all belong to the group: bulk stores (rows past
+    // the group would belong to the next group, so a warp whose rows cross
+    // the group's end takes the row-store path below)
     const int y = t.row0 + t.m * BM + q * 32;
     if constexpr (MODE == GU) {
 #pragma unroll 1
@@ -524,7 +525,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
         }
       }
     }
-  } else {
+  } else if (t.rows - t.m * BM - q * 32 > 0) {
     const bool valid = r_loc < t.rows;
     const int64_t row = (int64_t)t.row0 + r_loc;
     if constexpr (MODE == GU) {
@@ -627,12 +628,16 @@ __device__ bool wait_bounded_cluster(SharedState &st, uint32_t bar, uint32_t par
 // B_BOXES boxes of B at sa + kABytes (MN-major boxes: 64 K rows x 128 B).
 template <int A_BOXES, int B_BOXES>
 __device__ __forceinline__ void zero_tail_rows(uint8_t *sa_p, int valid, int lane) {
-  const int nz = (BK - valid) * (A_BOXES + B_BOXES);
-  for (int i = lane; i < nz * 8; i += 32) {
-    const int line = i >> 3, chunk = i & 7;
-    const int box = line / (BK - valid), r = valid + line % (BK - valid);
-    uint8_t *base = box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192;
-    *reinterpret_cast<uint4 *>(base + r * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+  // rows valid..BK-1 of every 64-row box are contiguous 128-byte lines, so
+  // each box's tail is one contiguous byte range (swizzling only permutes
+  // the 16-byte chunks inside a line)
+  const int nchunks = (BK - valid) * 8;
+#pragma unroll
+  for (int box = 0; box < A_BOXES + B_BOXES; ++box) {
+    uint8_t *tail = (box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192) +
+                    valid * 128;
+    for (int i = lane; i < nchunks; i += 32)
+      *reinterpret_cast<uint4 *>(tail + i * 16) = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async();
   __syncwarp();
