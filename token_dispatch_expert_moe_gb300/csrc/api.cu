@@ -274,7 +274,9 @@ moe_status_t moe_route_bwd(const moe_shape_t *shape, const void *x, const void *
     return MOE_ERR_INVALID_ARG;
   const bool sh = w_sg != nullptr;
   if ((dz != nullptr) != sh || (dw_sg != nullptr) != sh) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ws) || !aligned16(x) || !aligned16(W_r) || (sh && !aligned16(w_sg)) ||
+      !aligned16(dx_router) || (dx_in != nullptr && !aligned16(dx_in)))
+    return MOE_ERR_INVALID_ARG;   // 16-byte vector accesses
   const Layout L = layout(shape);
   RouteBwdArgs a{};
   a.T = shape->T; a.d = shape->d; a.E = shape->E; a.K = shape->K; a.dtype = shape->dtype;

@@ -8,7 +8,7 @@
 //      arithmetic as the forward); dp on the Top-K slots
 //      ((g - <g,w>) / Z with renorm, g without); dl = p (dp - <p,dp>).
 //   2. dx_kernel: dx_router[t] = dx_in[t] + sum_e dl[t,e] W_r[e] + dz[t] w_sg,
-//      register-tiled (4 tokens x 4 columns per thread);
+//      register-tiled (8 tokens x 4 columns per thread);
 //   3. wgrad_partial_kernel: per chunk of tokens, partial sums of dl^T x (and
 //      dz^T x), register-tiled; reduce_kernel adds the chunks in order:
 //      deterministic, no atomics.
@@ -51,75 +51,106 @@ __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
 }
 
 // dx_router[t, j] = dx_in[t, j] + sum_c dl[t, c] W[c, j]  (row c = E is w_sg
-// with dl = dz). A 64-token x 64-column tile per CTA with both operands in
-// shared memory (dl transposed, W converted to fp32); each thread computes 4
-// tokens x 4 columns, so one float4 of dl and one of W feed 16 FMAs. The sum
-// over c runs in a fixed order per output.
-constexpr int kDxT = 64, kDxJ = 64;
+// with dl = dz). A CTA takes 128 tokens and 256 columns: the dl tile stays in
+// shared memory in its natural [token][c] layout while four 64-column tiles
+// of W (converted to fp32) pass through. Each thread computes 8 tokens x 4
+// columns: per 4 values of c it reads 8 float4 of dl (broadcast within each
+// half-warp) and 4 float4 of W for 128 FMAs. The sum over c runs in
+// ascending order per output.
+constexpr int kDxT = 128, kDxJ = 64, kDxSub = 4;
+template <int CP> constexpr size_t dx_smem_bytes() { return (size_t)(kDxT + kDxJ) * CP * sizeof(float); }
+
 template <typename T, int CP>
 __global__ void __launch_bounds__(256) dx_kernel(RouteBwdArgs a) {
-  __shared__ __align__(16) float dlT[CP][kDxT];
-  __shared__ __align__(16) float Ws[CP][kDxJ];
+  extern __shared__ __align__(16) float dx_smem[];
+  float *dls = dx_smem;               // [kDxT][CP]
+  float *Ws = dx_smem + kDxT * CP;    // [CP][kDxJ]
+  constexpr int NV = Vec<T>::N;
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
   const int64_t t0 = (int64_t)blockIdx.x * kDxT;
-  const int j0 = blockIdx.y * kDxJ;
   const T *W = reinterpret_cast<const T *>(a.W_r);
   const T *wsg = reinterpret_cast<const T *>(a.w_sg);
-  for (int i = threadIdx.x; i < CP * kDxJ; i += blockDim.x) {
-    const int c = i / kDxJ, jj = i % kDxJ, j = j0 + jj;
-    float v = 0.0f;
-    if (c < C && j < a.d) v = to_f32(c < E ? W[(int64_t)c * a.d + j] : wsg[j]);
-    Ws[c][jj] = v;
-  }
-  for (int i = threadIdx.x; i < CP * kDxT; i += blockDim.x) {
-    const int tt = i / CP, c = i % CP;
+  for (int i = threadIdx.x; i < kDxT * CP; i += blockDim.x) {
+    const int tt = i / CP, c = i - tt * CP;
     const int64_t t = t0 + tt;
     float v = 0.0f;
     if (t < a.T && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
-    dlT[c][tt] = v;
+    dls[i] = v;
   }
-  __syncthreads();
-  const int tq = threadIdx.x >> 4;   // token quad 0..15
+  const int tq = threadIdx.x >> 4;   // token octet 0..15
   const int jq = threadIdx.x & 15;   // column quad 0..15
-  float acc[4][4];
+  for (int sub = 0; sub < kDxSub; ++sub) {
+    const int j0 = (blockIdx.y * kDxSub + sub) * kDxJ;
+    if (j0 >= a.d) break;   // the same for every thread of the CTA
+    __syncthreads();        // dl tile written; the previous W tile consumed
+    for (int i = threadIdx.x; i < CP * (kDxJ / NV); i += blockDim.x) {
+      const int c = i / (kDxJ / NV), jv = (i - c * (kDxJ / NV)) * NV;
+      const int j = j0 + jv;
+      float v[NV];
+      if (c < C && j < a.d) {   // d is a multiple of NV: a vector is all in or all out
+        load16<T>((c < E ? W + (int64_t)c * a.d : wsg) + j, v);
+      } else {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+        for (int q = 0; q < NV; ++q) v[q] = 0.0f;
+      }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[i][k] = 0.0f;
-#pragma unroll 4
-  for (int c = 0; c < CP; ++c) {
-    const float4 dv = *reinterpret_cast<const float4 *>(&dlT[c][tq * 4]);
-    const float4 wv = *reinterpret_cast<const float4 *>(&Ws[c][jq * 4]);
-    const float d4[4] = {dv.x, dv.y, dv.z, dv.w};
-    const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[i][k] = fmaf(d4[i], w4[k], acc[i][k]);
-  }
-  const int j = j0 + jq * 4;
-  if (j >= a.d) return;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t t = t0 + tq * 4 + i;
-    if (t >= a.T) break;
-    float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    if (a.dx_in != nullptr) {
-      const float4 xi = *reinterpret_cast<const float4 *>(a.dx_in + t * a.d + j);
-      o.x += xi.x; o.y += xi.y; o.z += xi.z; o.w += xi.w;
+      for (int q = 0; q < NV; q += 4)
+        *reinterpret_cast<float4 *>(&Ws[c * kDxJ + jv + q]) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
-    *reinterpret_cast<float4 *>(a.dx_router + t * a.d + j) = o;
+    __syncthreads();
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int n = 0; n < 4; ++n) acc[i][n] = 0.0f;
+#pragma unroll 2
+    for (int c = 0; c < CP; c += 4) {
+      float w[4][4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 wv = *reinterpret_cast<const float4 *>(&Ws[(c + k) * kDxJ + jq * 4]);
+        w[k][0] = wv.x; w[k][1] = wv.y; w[k][2] = wv.z; w[k][3] = wv.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 dv = *reinterpret_cast<const float4 *>(&dls[(tq * 8 + i) * CP + c]);
+        const float d4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int n = 0; n < 4; ++n) acc[i][n] = fmaf(d4[k], w[k][n], acc[i][n]);
+      }
+    }
+    const int j = j0 + jq * 4;
+    if (j < a.d) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int64_t t = t0 + tq * 8 + i;
+        if (t >= a.T) break;
+        float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        if (a.dx_in != nullptr) {
+          const float4 xi = *reinterpret_cast<const float4 *>(a.dx_in + t * a.d + j);
+          o.x += xi.x; o.y += xi.y; o.z += xi.z; o.w += xi.w;
+        }
+        *reinterpret_cast<float4 *>(a.dx_router + t * a.d + j) = o;
+      }
+    }
   }
 }
 
 // Partial sums over one chunk of tokens of dl^T x (row E: dz^T x): a
 // CP x 256 tile per CTA (CP a multiple of 8, rows >= C zero), each thread
-// CP/8 rows x 8 columns. Per token a thread reads CP/8 dl values and one
-// 16-byte x vector from shared memory for CP FMAs.
+// CP/8 rows x 8 columns. Per token a thread reads CP/8 dl values and two
+// float4 of x from shared memory for CP FMAs. Tokens pass through shared
+// memory 32 at a time; the next 32 are loaded into registers (16-byte
+// vectors of x) while the current ones are summed.
 template <typename T, int CP>
-__global__ void __launch_bounds__(256) wgrad_partial_kernel(RouteBwdArgs a, int64_t chunk) {
-  constexpr int RPT = CP / 8;   // rows of the tile per thread
+__global__ void __launch_bounds__(256, 2) wgrad_partial_kernel(RouteBwdArgs a, int64_t chunk) {
+  constexpr int RPT = CP / 8;                    // rows of the tile per thread
+  constexpr int NV = Vec<T>::N;                  // elements of x per 16-byte vector
+  constexpr int XV = 32 * kCols / NV / 256;      // x vectors per thread per slab
+  constexpr int DV = (32 * CP + 255) / 256;      // dl values per thread per slab
   __shared__ __align__(16) float dls[32][CP];
   __shared__ __align__(16) float xs[32][kCols];
   const int E = a.E;
@@ -130,26 +161,55 @@ __global__ void __launch_bounds__(256) wgrad_partial_kernel(RouteBwdArgs a, int6
   const int rg = threadIdx.x >> 5;   // row group 0..7 (one per warp)
   const int jo = threadIdx.x & 31;   // column octet 0..31
   const T *x = reinterpret_cast<const T *>(a.x);
+  uint4 xr[XV];
+  float dr[DV];
+  auto fetch = [&](int64_t s0) {
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int idx = threadIdx.x + v * 256;
+      const int tt = idx / (kCols / NV), jv = (idx % (kCols / NV)) * NV;
+      const int64_t t = s0 + tt;
+      xr[v] = (t < te && j0 + jv < a.d)   // d is a multiple of NV
+                  ? *reinterpret_cast<const uint4 *>(x + t * a.d + j0 + jv)
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int q = 0; q < DV; ++q) {
+      const int idx = threadIdx.x + q * 256;
+      const int tt = idx / CP, c = idx % CP;
+      const int64_t t = s0 + tt;
+      float v = 0.0f;
+      if (idx < 32 * CP && t < te && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
+      dr[q] = v;
+    }
+  };
+  fetch(tb);
   float acc[RPT][8];
 #pragma unroll
   for (int r = 0; r < RPT; ++r)
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[r][k] = 0.0f;
   for (int64_t s0 = tb; s0 < te; s0 += 32) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < 32 * CP; i += blockDim.x) {
-      const int tt = i / CP, c = i % CP;
-      const int64_t t = s0 + tt;
-      float v = 0.0f;
-      if (t < te && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
-      dls[tt][c] = v;
+    __syncthreads();   // the previous slab is consumed
+#pragma unroll
+    for (int v = 0; v < XV; ++v) {
+      const int idx = threadIdx.x + v * 256;
+      const int tt = idx / (kCols / NV), jv = (idx % (kCols / NV)) * NV;
+      float f[NV];
+      const T *src = reinterpret_cast<const T *>(&xr[v]);
+#pragma unroll
+      for (int q = 0; q < NV; ++q) f[q] = to_f32(src[q]);
+#pragma unroll
+      for (int q = 0; q < NV; q += 4)
+        *reinterpret_cast<float4 *>(&xs[tt][jv + q]) = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
     }
-    for (int i = threadIdx.x; i < 32 * kCols; i += blockDim.x) {
-      const int tt = i / kCols, jj = i % kCols;
-      const int64_t t = s0 + tt;
-      xs[tt][jj] = (t < te && j0 + jj < a.d) ? to_f32(x[t * a.d + j0 + jj]) : 0.0f;
+#pragma unroll
+    for (int q = 0; q < DV; ++q) {
+      const int idx = threadIdx.x + q * 256;
+      if (idx < 32 * CP) dls[idx / CP][idx % CP] = dr[q];
     }
     __syncthreads();
+    if (s0 + 32 < te) fetch(s0 + 32);   // in flight while this slab is summed
     const int n = (int)min((int64_t)32, te - s0);
     for (int tt = 0; tt < n; ++tt) {
       const float4 x0 = *reinterpret_cast<const float4 *>(&xs[tt][jo * 8]);
@@ -213,17 +273,21 @@ size_t route_bwd_workspace_bytes(int64_t T, int d, int E) {
   return dl + (size_t)kChunks * (E + 1) * d * sizeof(float);
 }
 
+template <typename T, int CP>
+void launch_cp_t(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk) {
+  constexpr int kSubCols = kDxJ * kDxSub;
+  dim3 gdx((unsigned)((a.T + kDxT - 1) / kDxT), (unsigned)((a.d + kSubCols - 1) / kSubCols));
+  dim3 gw((unsigned)nchunk, (unsigned)((a.d + kCols - 1) / kCols));
+  auto k = dx_kernel<T, CP>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dx_smem_bytes<CP>());
+  k<<<gdx, 256, dx_smem_bytes<CP>(), s>>>(a);
+  wgrad_partial_kernel<T, CP><<<gw, 256, 0, s>>>(a, chunk);
+}
+
 template <int CP>
 void launch_cp(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk) {
-  dim3 gdx((unsigned)((a.T + kDxT - 1) / kDxT), (unsigned)((a.d + kDxJ - 1) / kDxJ));
-  dim3 gw((unsigned)nchunk, (unsigned)((a.d + kCols - 1) / kCols));
-  if (a.dtype == MOE_BF16) {
-    dx_kernel<__nv_bfloat16, CP><<<gdx, kCols, 0, s>>>(a);
-    wgrad_partial_kernel<__nv_bfloat16, CP><<<gw, kCols, 0, s>>>(a, chunk);
-  } else {
-    dx_kernel<float, CP><<<gdx, kCols, 0, s>>>(a);
-    wgrad_partial_kernel<float, CP><<<gw, kCols, 0, s>>>(a, chunk);
-  }
+  if (a.dtype == MOE_BF16) launch_cp_t<__nv_bfloat16, CP>(a, s, chunk, nchunk);
+  else launch_cp_t<float, CP>(a, s, chunk, nchunk);
 }
 
 cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
@@ -234,6 +298,7 @@ cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
   if (C <= 8) launch_cp<8>(a, s, chunk, nchunk);
   else if (C <= 16) launch_cp<16>(a, s, chunk, nchunk);
   else if (C <= 32) launch_cp<32>(a, s, chunk, nchunk);
+  else if (C <= 64) launch_cp<64>(a, s, chunk, nchunk);
   else launch_cp<72>(a, s, chunk, nchunk);
   const int64_t n = (int64_t)C * a.d;
   reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, nchunk);
