@@ -48,9 +48,9 @@ template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> { static constexpr int N = 8; };
 template <> struct Vec<float> { static constexpr int N = 4; };
 
+// 16 loaded bytes (8 bf16 or 4 fp32) to fp32
 template <typename T>
-__device__ __forceinline__ void load16(const T *p, float (&v)[Vec<T>::N]) {
-  uint4 u = *reinterpret_cast<const uint4 *>(p);
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&v)[Vec<T>::N]) {
   if constexpr (Vec<T>::N == 8) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
@@ -64,6 +64,11 @@ __device__ __forceinline__ void load16(const T *p, float (&v)[Vec<T>::N]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = f[i];
   }
+}
+
+template <typename T>
+__device__ __forceinline__ void load16(const T *p, float (&v)[Vec<T>::N]) {
+  unpack16<T>(*reinterpret_cast<const uint4 *>(p), v);
 }
 
 template <typename T>

@@ -216,21 +216,28 @@ __global__ void __launch_bounds__(256) unpermute_kernel(UnpermuteArgs a) {
 }
 
 // dYp[row] = w * dout[t]; dw[t,k] = <dout[t], Yp[row]>; shared: dYs, dz.
+// One CTA per token. Per 16-byte column vector a thread first issues the
+// loads of all K expert rows (and Ys), then computes and stores, so that up to
+// K + 2 loads per thread are in flight. The K (+1) dot products are reduced
+// with one butterfly per warp and then over the warps in order (fixed order:
+// bitwise reproducible).
 template <typename T>
 __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
   constexpr int N = Vec<T>::N;
   const int64_t t = blockIdx.x;
   const int K = a.K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ int32_t rows[8];
   __shared__ float wts[8];
   __shared__ float gate;
-  __shared__ float red[32];
+  __shared__ float red[8][9];   // [warp][slot]; slot 8 = shared expert
   if (threadIdx.x < K) {
     rows[threadIdx.x] = a.row_of[t * K + threadIdx.x];
     wts[threadIdx.x] = a.topk_w[t * K + threadIdx.x];
   }
   if (threadIdx.x == 0 && a.Ys != nullptr) gate = 1.0f / (1.0f + __expf(-a.gate_logit[t]));
   __syncthreads();
+  const bool shared = a.Ys != nullptr;
   const T *Yp = reinterpret_cast<const T *>(a.Yp);
   const T *dout = reinterpret_cast<const T *>(a.dout);
   T *dYp = reinterpret_cast<T *>(a.dYp);
@@ -238,26 +245,31 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
 #pragma unroll
   for (int k = 0; k < 9; ++k) dot[k] = 0.0f;
   for (int v = threadIdx.x * N; v < a.d; v += blockDim.x * N) {
+    uint4 graw, yraw[9];
+    graw = *reinterpret_cast<const uint4 *>(dout + t * a.d + v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < K && rows[k] >= 0)
+        yraw[k] = *reinterpret_cast<const uint4 *>(Yp + (int64_t)rows[k] * a.d + v);
+    if (shared) yraw[8] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.Ys) + t * a.d + v);
     float g[N];
-    load16<T>(dout + t * a.d + v, g);
+    unpack16<T>(graw, g);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      if (k >= K) break;
-      const int32_t r = rows[k];
-      if (r < 0) continue;
+      if (k >= K || rows[k] < 0) continue;
       float y[N], o[N];
-      load16<T>(Yp + (int64_t)r * a.d + v, y);
+      unpack16<T>(yraw[k], y);
       const float w = wts[k];
 #pragma unroll
       for (int i = 0; i < N; ++i) {
         dot[k] = fmaf(g[i], y[i], dot[k]);
         o[i] = w * g[i];
       }
-      store16<T>(dYp + (int64_t)r * a.d + v, o);
+      store16<T>(dYp + (int64_t)rows[k] * a.d + v, o);
     }
-    if (a.Ys != nullptr) {
+    if (shared) {
       float y[N], o[N];
-      load16<T>(reinterpret_cast<const T *>(a.Ys) + t * a.d + v, y);
+      unpack16<T>(yraw[8], y);
 #pragma unroll
       for (int i = 0; i < N; ++i) {
         dot[8] = fmaf(g[i], y[i], dot[8]);
@@ -266,13 +278,22 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
       store16<T>(reinterpret_cast<T *>(a.dYs) + t * a.d + v, o);
     }
   }
-  for (int k = 0; k < K; ++k) {
-    const float s = block_sum(dot[k], red);
-    if (threadIdx.x == 0) a.dw[t * K + k] = rows[k] >= 0 ? s : 0.0f;
+#pragma unroll
+  for (int k = 0; k < 9; ++k) {
+    const float s = warp_sum(dot[k]);
+    if (lane == 0) red[warp][k] = s;
   }
-  if (a.Ys != nullptr) {
-    const float s = block_sum(dot[8], red);
-    if (threadIdx.x == 0) a.dz[t] = gate * (1.0f - gate) * s;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  if (threadIdx.x < K) {
+    const int k = threadIdx.x;
+    float s = 0.0f;
+    for (int w = 0; w < nw; ++w) s += red[w][k];
+    a.dw[t * K + k] = rows[k] >= 0 ? s : 0.0f;
+  } else if (threadIdx.x == 32 && shared) {
+    float s = 0.0f;
+    for (int w = 0; w < nw; ++w) s += red[w][8];
+    a.dz[t] = gate * (1.0f - gate) * s;
   }
 }
 
