@@ -260,7 +260,7 @@ def main():
     dout = to_device(inp["dout"]) if cfg.backward else None
     stream = torch.cuda.current_stream()
 
-    ffn_ev, perm_ev, unperm_ev = [], [], []
+    ffn_ev, perm_ev, unperm_ev, ffn_bwd_ev = [], [], [], []
 
     def step(x, out, record=False):
         c, s, ws = cfg_r, layer.shape, layer.ws
@@ -283,7 +283,10 @@ def main():
         L.moe_unpermute(s, layer.Yp, layer.row_of, layer.topk_w, layer.Ys, layer.gate_logit, out)
         if record: e[5].record(stream)
         if c.backward:
-            layer.backward(dout)
+            eb = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) if record else None
+            layer.backward(dout, ffn_events=eb)
+            if record:
+                ffn_bwd_ev.append(eb)
         if record:
             perm_ev.append((e[0], e[1]))
             ffn_ev.append((e[2], e[3]))
@@ -417,6 +420,11 @@ def main():
                 "hbm_peak_GBps": hbm_peak,
             },
         }
+        if ffn_bwd_ev:   # routed experts' dgrad + wgrad: 12 N d F FLOP per call
+            bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_bwd_ev)
+            bwd_tf = 12.0 * n_kept * cfg.d * cfg.F / (bwd_ms * 1e-3) / 1e12
+            line["stages"].update(ffn_bwd_ms=bwd_ms, ffn_bwd_tflops=bwd_tf,
+                                  ffn_bwd_frac=bwd_tf / bf16_peak)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_throughput(cfg, inp)
         print(json.dumps(line), flush=True)

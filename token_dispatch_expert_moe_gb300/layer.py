@@ -99,14 +99,20 @@ class MoELayer:
                         stream)
         return self.out
 
-    def backward(self, dout: torch.Tensor, stream=None) -> dict:
+    def backward(self, dout: torch.Tensor, stream=None, ffn_events=None) -> dict:
+        """ffn_events: optional (start, end) CUDA events recorded on the current
+        stream around the routed experts' moe_expert_ffn_bwd call."""
         c, s, w = self.cfg, self.shape, self.w
         L.moe_unpermute_bwd(s, dout, self.Yp, self.row_of, self.topk_w, self.Ys, self.gate_logit,
                             self.dYp, self.dw, self.dYs if self.shared else None,
                             self.dz if self.shared else None, stream)
+        if ffn_events is not None:
+            ffn_events[0].record()
         L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.dYp,
                              self.Xp, self.A_save, self.H, w["W_gu"], w["W_down"], self.dA,
                              self.dXp, self.dW_gu, self.dW_down, self.ws, stream)
+        if ffn_events is not None:
+            ffn_events[1].record()
         dx_in = None
         if self.shared:
             L.moe_expert_ffn_bwd(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, self.dYs, self.x,
