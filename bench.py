@@ -170,15 +170,17 @@ def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = Non
 
 # ---------------------------------------------------------------------------
 
-def launches_per_step(cfg) -> int:
+def launches_per_step(cfg, etp: int = 1) -> int:
     n = (2 if cfg.dtype == "bf16" else 1)  # router: logits GEMM + Top-K (fp32: one fused kernel)
     n += 1 if cfg.drop else 0             # capacity
     n += 3                                 # map count, map scatter, row copy
-    n += 2 + (2 if cfg.Fs else 0)          # grouped GEMMs (routed [+ shared])
+    n += 2 * etp + (1 if etp > 1 else 0)   # routed grouped GEMMs per F-shard [+ partial sum]
+    n += 2 if cfg.Fs else 0                # shared expert
     n += 1                                 # un-permute
     if cfg.backward:
         n += 1                             # un-permute backward
-        n += 4 + (4 if cfg.Fs else 0)      # dH, dX, dW_down, dW_gu GEMMs
+        n += 4 * etp + (1 if etp > 1 else 0)   # dH, dX, dW_down, dW_gu per shard [+ dXp sum]
+        n += 4 if cfg.Fs else 0
         n += 4 + (1 if cfg.bias else 0)    # router backward
         n += 1                             # permute backward
     return n
@@ -222,6 +224,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--etp", type=int, default=1,
+                    help="run the routed experts F-split into this many shards (the arithmetic "
+                         "of an expert-tensor-parallel group, on one GPU)")
     ap.add_argument("--override", default="",
                     help="profiling cases only: comma-separated field=value changes to the "
                          "workload, e.g. T=4096,E=16 (the JSON line then names the changed shape)")
@@ -254,7 +259,7 @@ def main():
     cfg_r = dataclasses.replace(cfg, seed=cfg.seed + rank)   # each replica its own batch
     inp = make_inputs(cfg_r)
     w = {k: to_device(v) for k, v in inp.items() if k not in ("x", "dout")}
-    layer = MoELayer(cfg_r, w)
+    layer = MoELayer(cfg_r, w, etp=args.etp)
     x = to_device(inp["x"])
     layer.x = x   # the backward reads the forward's tokens
     dout = to_device(inp["dout"]) if cfg.backward else None
@@ -273,8 +278,7 @@ def main():
                       layer.counts, layer.offsets, ws)
         if record: e[1].record(stream)
         if record: e[2].record(stream)
-        L.moe_expert_ffn(layer.dtype_code, c.T * c.K, c.d, c.F, c.E, layer.offsets, layer.Xp,
-                         w["W_gu"], w["W_down"], layer.A_save, layer.H, layer.Yp, ws)
+        layer.routed_ffn()
         if record: e[3].record(stream)
         if c.Fs:
             L.moe_expert_ffn(layer.dtype_code, c.T, c.d, c.Fs, 1, layer.off1, x, w["Ws_gu"],
@@ -401,11 +405,11 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * agg["seconds"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic (seeded normal inputs, random-init weights)",
-            "config": workload_config(cfg),
+            "config": dict(workload_config(cfg), **({"etp_shards": args.etp} if args.etp > 1 else {})),
             "clocks": clk,
             "e2e": {"value": e2e["value"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step(cfg) * args.steps,
+            "gpu_launches": launches_per_step(cfg, args.etp) * args.steps,
             "roofline": {"kernel": "grouped SwiGLU GEMM (moe_expert_ffn: gate/up + down)",
                          "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,

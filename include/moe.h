@@ -230,6 +230,20 @@ moe_status_t moe_permute_bwd(const moe_shape_t *shape, const float *dXp,
                              const int32_t *row_of, const float *dx_add, float *dx,
                              moe_stream_t stream);
 
+/* Sum of partial results in part order (the arithmetic of a ReduceScatter-V
+ * over an expert-tensor-parallel group, done on one GPU): out[i] =
+ * dtype(((partials[0][i] + partials[1][i]) + ...) + partials[n_parts-1][i]),
+ * fp32 additions, one rounding. MoE Parallel Folding study notes, "method
+ * overview": ETP splits an expert's FFN dimension over ranks and sums the
+ * partial outputs (ReduceScatter-V); here the F-shards of one expert run as
+ * separate moe_expert_ffn calls and this call adds their outputs.
+ *   partials [n_parts, rows, d] dtype, contiguous; out [rows, d] dtype (may
+ *   not alias partials). dtype MOE_BF16 or MOE_F32; 1 <= n_parts <= 16;
+ *   d a multiple of 8 (bf16) or 4 (fp32); pointers 16-byte aligned.
+ * Errors: MOE_ERR_INVALID_ARG for NULL/misaligned pointers or bad sizes.    */
+moe_status_t moe_sum_partials(int32_t dtype, int32_t n_parts, int64_t rows, int32_t d,
+                              const void *partials, void *out, moe_stream_t stream);
+
 /* Router backward. g = dw [T,K]; renorm: dp_j = (g_j - sum_k g_k w_k) / Z on
  * the Top-K (Z = sum of topk_prob), else dp = g there; dp = 0 elsewhere;
  * p = softmax(logits) as in moe_route_topk; dl_i = p_i (dp_i - sum_j p_j dp_j).

@@ -34,7 +34,12 @@ formula, tie rules, rounding points. The readings used here are:
     flat token order; keep the highest-probability assignments (raw softmax p),
     ties to the lower token index; kept weights are not renormalised again;
   * permuted order: expert-major, token-ascending inside an expert, compact;
-  * an optional shared expert adds sigmoid(x . w_sg) * SwiGLU_shared(x).
+  * an optional shared expert adds sigmoid(x . w_sg) * SwiGLU_shared(x);
+  * expert tensor parallelism (the F-split of an expert over a group, whose
+    partial outputs a ReduceScatter-V sums): each shard's partial output is
+    stored in the activation dtype, the partials are added in shard order
+    with fp32 additions and rounded once; in the backward each shard's fp32
+    dXp partial is added the same way.
 
 Precision. Arithmetic is fp64 everywhere except the routing decision chain,
 which both sides must take on identical bits: the softmax below is specified
@@ -315,6 +320,54 @@ def expert_ffn(Xp, offsets, W_gu, W_down, dtype="bf16", mirror=True, rows=None):
 
 
 # --------------------------------------------------------------------------
+# f4: the expert FFN F-split over an expert-tensor-parallel group
+#     [notes/method: ETP shards the expert's FFN dimension over ranks; a
+#      ReduceScatter-V sums the partial outputs]
+
+def fsplit_weights(W_gu, W_down, shards: int, s: int):
+    """Shard s of `shards`: gate rows [s F/P, (s+1) F/P) and the same up rows
+    of W_gu [E,2F,d] (stacked gate then up, as in the full layout), and the
+    matching columns of W_down [E,d,F]."""
+    F = W_gu.shape[1] // 2
+    Fl = F // shards
+    cols = np.arange(s * Fl, (s + 1) * Fl)
+    return W_gu[:, np.concatenate([cols, F + cols])], W_down[:, :, cols]
+
+
+def sum_partials(parts, mirror=True):
+    """Sum of shard partials in shard order; with mirror every addition is an
+    fp32 addition (the partials are fp32-representable values)."""
+    r32 = f32_rounder(mirror)
+    acc = np.asarray(parts[0], dtype=np.float64)
+    for p in parts[1:]:
+        acc = r32(acc + np.asarray(p, dtype=np.float64))
+    return acc
+
+
+def expert_ffn_fsplit(Xp, offsets, W_gu, W_down, shards: int, dtype="bf16", mirror=True):
+    """Grouped SwiGLU FFN with F split into `shards`: every shard is a full
+    grouped FFN on its gate/up rows and W_down columns; its partial output
+    is stored in the activation dtype (the partials a ReduceScatter-V adds);
+    Yp = rnd(sum of the partials in shard order, fp32 additions). A_save and
+    H are the shards' columns put back in the full layout (SwiGLU acts per
+    column, so they equal the unsplit ones)."""
+    rnd = act_rounder(dtype, mirror)
+    F = W_gu.shape[1] // 2
+    Fl = F // shards
+    n = Xp.shape[0]
+    A = np.full((n, 2 * F), np.nan)
+    H = np.full((n, F), np.nan)
+    parts = []
+    for s in range(shards):
+        Wg, Wd = fsplit_weights(W_gu, W_down, shards, s)
+        a, h, y = expert_ffn(Xp, offsets, Wg, Wd, dtype, mirror)
+        cols = np.arange(s * Fl, (s + 1) * Fl)
+        A[:, cols], A[:, F + cols], H[:, cols] = a[:, :Fl], a[:, Fl:], h
+        parts.append(y)
+    return A, H, rnd(sum_partials(parts, mirror))
+
+
+# --------------------------------------------------------------------------
 # a9: un-permute and combine  [notes/method: un-permutation restores order]
 
 def sigmoid(z):
@@ -408,6 +461,32 @@ def expert_ffn_bwd(dYp, Xp, A_save, H_save, offsets, W_gu, W_down,
     return dXp, dWgu, dWd, dA
 
 
+def expert_ffn_bwd_fsplit(dYp, Xp, A_save, H_save, offsets, W_gu, W_down, shards: int,
+                         dtype="bf16", mirror=True):
+    """Backward of expert_ffn_fsplit: every shard sees the whole dYp (the
+    backward of the ReduceScatter-V is a gather); each shard's dXp partial is
+    fp32 and dXp is their sum in shard order (fp32 additions); the weight
+    gradients and dA are per shard, put back in the full layout."""
+    E, twoF, d = W_gu.shape
+    F = twoF // 2
+    Fl = F // shards
+    n = Xp.shape[0]
+    dWgu = np.zeros((E, twoF, d))
+    dWd = np.zeros((E, d, F))
+    dA = np.zeros((n, twoF))
+    parts = []
+    for s in range(shards):
+        cols = np.arange(s * Fl, (s + 1) * Fl)
+        Wg, Wd = fsplit_weights(W_gu, W_down, shards, s)
+        A_s = np.concatenate([A_save[:, cols], A_save[:, F + cols]], axis=1)
+        dX, dwgu, dwd, da = expert_ffn_bwd(dYp, Xp, A_s, H_save[:, cols], offsets, Wg, Wd,
+                                           dtype, mirror)
+        parts.append(dX)
+        dWgu[:, cols], dWgu[:, F + cols], dWd[:, :, cols] = dwgu[:, :Fl], dwgu[:, Fl:], dwd
+        dA[:, cols], dA[:, F + cols] = da[:, :Fl], da[:, Fl:]
+    return sum_partials(parts, mirror), dWgu, dWd, dA
+
+
 def permute_bwd(dXp, row_of, dx_add=None, mirror=True):
     """a13. dx[t] = sum_{kept k} dXp[row_of[t,k]] (+ dx_add[t]), fp32."""
     T, K = row_of.shape
@@ -475,13 +554,18 @@ def route(cfg, inp, mirror=True, logits=None):
             "topk_w": w, "keep": keep}
 
 
-def layer_forward(cfg, inp, mirror=True, logits=None):
+def layer_forward(cfg, inp, mirror=True, logits=None, etp=1):
     """Full forward: route, drop, map, permute, expert FFN, (shared expert),
-    un-permute with the weighted Top-K combine."""
+    un-permute with the weighted Top-K combine. etp > 1: the routed experts
+    F-split into etp shards (expert_ffn_fsplit)."""
     r = route(cfg, inp, mirror=mirror, logits=logits)
     counts, offsets, row_of, src_of, n_kept = build_map(r["topk_idx"], r["keep"], cfg.E)
     Xp = permute(inp["x"], src_of, cfg.K)
-    A, H, Yp = expert_ffn(Xp, offsets, inp["W_gu"], inp["W_down"], cfg.dtype, mirror)
+    if etp > 1:
+        A, H, Yp = expert_ffn_fsplit(Xp, offsets, inp["W_gu"], inp["W_down"], etp, cfg.dtype,
+                                     mirror)
+    else:
+        A, H, Yp = expert_ffn(Xp, offsets, inp["W_gu"], inp["W_down"], cfg.dtype, mirror)
     out = dict(r, counts=counts, offsets=offsets, row_of=row_of, src_of=src_of,
                n_kept=n_kept, Xp=Xp, A_save=A, H_save=H, Yp=Yp)
     Ys = z = None
@@ -495,13 +579,18 @@ def layer_forward(cfg, inp, mirror=True, logits=None):
     return out
 
 
-def layer_backward(cfg, inp, fwd, mirror=True):
-    """Full backward for upstream gradient inp['dout']."""
+def layer_backward(cfg, inp, fwd, mirror=True, etp=1):
+    """Full backward for upstream gradient inp['dout'] (etp as in layer_forward)."""
     ub = unpermute_bwd(inp["dout"], fwd["Yp"], fwd["row_of"], fwd["topk_w"],
                        fwd.get("Ys"), fwd.get("gate_logit"), cfg.dtype, mirror)
-    dXp, dWgu, dWd, dA = expert_ffn_bwd(ub["dYp"], fwd["Xp"], fwd["A_save"], fwd["H_save"],
-                                        fwd["offsets"], inp["W_gu"], inp["W_down"],
-                                        cfg.dtype, mirror)
+    if etp > 1:
+        dXp, dWgu, dWd, dA = expert_ffn_bwd_fsplit(ub["dYp"], fwd["Xp"], fwd["A_save"],
+                                                   fwd["H_save"], fwd["offsets"], inp["W_gu"],
+                                                   inp["W_down"], etp, cfg.dtype, mirror)
+    else:
+        dXp, dWgu, dWd, dA = expert_ffn_bwd(ub["dYp"], fwd["Xp"], fwd["A_save"], fwd["H_save"],
+                                            fwd["offsets"], inp["W_gu"], inp["W_down"],
+                                            cfg.dtype, mirror)
     g = {"dYp": ub["dYp"], "dw": ub["dw"], "dXp": dXp, "dA": dA,
          "dW_gu": dWgu, "dW_down": dWd}
     dx_add = None

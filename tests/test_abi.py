@@ -81,3 +81,17 @@ def test_invalid_arguments_rejected_on_host(L):
         L.moe_route_bwd(s, fake, fake, fake, fake, fake, fake, fake, fake, None, None, fake, None,
                         None, fake, fake, 0)
     assert e.value.code == 1
+    with pytest.raises(L.MoEError) as e:   # route_bwd: misaligned dx_router
+        L.moe_route_bwd(s, fake, fake, None, fake, fake, fake, fake, fake, None, None, fake, None,
+                        None, fake + 4, fake, 0)
+    assert e.value.code == 1
+    for args in [(3, 2, 8, 64, fake, fake + (1 << 16)),      # unknown dtype
+                 (1, 0, 8, 64, fake, fake + (1 << 16)),      # no parts
+                 (1, 17, 8, 64, fake, fake + (1 << 16)),     # too many parts
+                 (1, 2, 8, 60, fake, fake + (1 << 16)),      # d % 8 for bf16
+                 (1, 2, 8, 64, fake + 2, fake + (1 << 16)),  # misaligned partials
+                 (1, 2, 8, 64, fake, fake + 1024)]:          # out inside partials
+        with pytest.raises(L.MoEError) as e:
+            L.moe_sum_partials(*args, 0)
+        assert e.value.code == 1, args
+    L.moe_sum_partials(1, 2, 0, 64, None, None, 0)   # zero rows: nothing to do

@@ -183,3 +183,51 @@ def test_backward_matches_finite_differences(variant):
             num = (lp - lm) / (2 * h)
             ana = g[gname][i]
             assert abs(num - ana) <= 1e-6 * max(1.0, abs(num)), (pname, i, num, ana)
+
+
+# ---- expert F-split over an expert-tensor-parallel group (f4) ----
+
+@pytest.mark.parametrize("shards", [2, 3])
+def test_fsplit_is_the_unsplit_ffn_in_exact_arithmetic(shards):
+    """Without rounding (fp64), the F-split FFN equals the unsplit one: the
+    down projection is linear in the hidden units, and SwiGLU acts per unit.
+    A wrong gate/up row pairing or W_down column choice breaks this."""
+    rng = np.random.default_rng(7)
+    E, n, d, F = 3, 40, 10, 12
+    Xp = rng.standard_normal((n, d))
+    offsets = np.array([0, 17, 17, 40], dtype=np.int32)
+    W_gu = rng.standard_normal((E, 2 * F, d)) / np.sqrt(d)
+    W_down = rng.standard_normal((E, d, F)) / np.sqrt(F)
+    A, H, Y = O.expert_ffn(Xp, offsets, W_gu, W_down, "f32", mirror=False)
+    As, Hs, Ys = O.expert_ffn_fsplit(Xp, offsets, W_gu, W_down, shards, "f32", mirror=False)
+    assert np.array_equal(As, A) and np.array_equal(Hs, H)
+    assert np.abs(Ys - Y).max() <= 1e-12 * np.abs(Y).max()
+    dYp = rng.standard_normal((n, d))
+    dX, dWgu, dWd, dA = O.expert_ffn_bwd(dYp, Xp, A, H, offsets, W_gu, W_down, "f32", mirror=False)
+    sX, sWgu, sWd, sA = O.expert_ffn_bwd_fsplit(dYp, Xp, A, H, offsets, W_gu, W_down, shards,
+                                                "f32", mirror=False)
+    assert np.array_equal(sA, dA) and np.array_equal(sWgu, dWgu) and np.array_equal(sWd, dWd)
+    assert np.abs(sX - dX).max() <= 1e-12 * np.abs(dX).max()
+
+
+def test_fsplit_one_shard_is_expert_ffn():
+    rng = np.random.default_rng(8)
+    Xp = rng.standard_normal((20, 8)).astype(np.float32)
+    offsets = np.array([0, 9, 20], dtype=np.int32)
+    W_gu = (rng.standard_normal((2, 12, 8)) / 3).astype(np.float32)
+    W_down = (rng.standard_normal((2, 8, 6)) / 3).astype(np.float32)
+    a = O.expert_ffn(Xp, offsets, W_gu, W_down, "bf16")
+    b = O.expert_ffn_fsplit(Xp, offsets, W_gu, W_down, 1, "bf16")
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_sum_partials_adds_in_shard_order_in_fp32():
+    """(a + b) + c differs from a + (b + c) in fp32 here: the oracle must take
+    the shard order with an fp32 rounding after every addition."""
+    a, b, c = np.float64(1.0), np.float64(2.0 ** -24), np.float64(2.0 ** -24)
+    left = O.sum_partials([np.array([a]), np.array([b]), np.array([c])])
+    assert left[0] == 1.0                         # each tiny addend is rounded away
+    right = O.sum_partials([np.array([b]), np.array([c]), np.array([a])])
+    assert right[0] == 1.0 + 2.0 ** -23           # the two tiny addends first survive
+    assert O.sum_partials([np.array([a]), np.array([b])], mirror=False)[0] == 1.0 + 2.0 ** -24

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_expert_ffn_bwd": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            _P, _P, _P, _P],
     "moe_permute_bwd": [_S, _P, _P, _P, _P, _P],
+    "moe_sum_partials": [_I32, _I32, _I64, _I32, _P, _P, _P],
     "moe_route_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_clear_status": [_P, _P],
     "moe_get_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
@@ -170,6 +171,10 @@ def moe_expert_ffn_bwd(dtype, max_rows, d, F, n_groups, offsets, dYp, Xp, A_save
 def moe_permute_bwd(shape, dXp, row_of, dx_add, dx, stream=None):
     _call("moe_permute_bwd", ctypes.byref(shape), _ptr(dXp), _ptr(row_of), _ptr(dx_add), _ptr(dx),
           _stream(stream))
+
+
+def moe_sum_partials(dtype, n_parts, rows, d, partials, out, stream=None):
+    _call("moe_sum_partials", dtype, n_parts, rows, d, _ptr(partials), _ptr(out), _stream(stream))
 
 
 def moe_route_bwd(shape, x, W_r, w_sg, logits, topk_idx, topk_prob, topk_w, dw, dz, dx_in, dW_r,

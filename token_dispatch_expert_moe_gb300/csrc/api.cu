@@ -264,6 +264,21 @@ moe_status_t moe_permute_bwd(const moe_shape_t *shape, const float *dXp, const i
                                         (cudaStream_t)stream));
 }
 
+moe_status_t moe_sum_partials(int32_t dtype, int32_t n_parts, int64_t rows, int32_t d,
+                              const void *partials, void *out, moe_stream_t stream) {
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (n_parts < 1 || n_parts > 16 || rows < 0 || d < 1) return MOE_ERR_INVALID_ARG;
+  if (d % (dtype == MOE_BF16 ? 8 : 4) != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!partials || !out || !aligned16(partials) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const size_t b = dtype == MOE_BF16 ? 2 : 4;
+  const char *p0 = static_cast<const char *>(partials), *o0 = static_cast<const char *>(out);
+  const size_t part = (size_t)rows * d * b;
+  if (o0 < p0 + part * n_parts && p0 < o0 + part) return MOE_ERR_INVALID_ARG;   // aliasing
+  return cuda_status(launch_sum_partials(dtype, n_parts, rows, d, partials, out,
+                                         (cudaStream_t)stream));
+}
+
 moe_status_t moe_route_bwd(const moe_shape_t *shape, const void *x, const void *W_r,
                            const void *w_sg, const float *logits, const int32_t *topk_idx,
                            const float *topk_prob, const float *topk_w, const float *dw,

@@ -160,6 +160,8 @@ struct UnpermuteArgs {
 };
 cudaError_t launch_unpermute(const UnpermuteArgs &a, cudaStream_t s);
 cudaError_t launch_unpermute_bwd(const UnpermuteArgs &a, cudaStream_t s);
+cudaError_t launch_sum_partials(int dtype, int n_parts, int64_t rows, int d, const void *partials,
+                                void *out, cudaStream_t s);
 cudaError_t launch_permute_bwd(int64_t T, int d, int K, const float *dXp,
                                const int32_t *row_of, const float *dx_add, float *dx,
                                cudaStream_t s);

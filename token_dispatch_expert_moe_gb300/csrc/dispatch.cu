@@ -297,6 +297,28 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
   }
 }
 
+// out = sum over parts (in part order, fp32) of partials[p]; one 16-byte
+// vector per thread and iteration, grid-stride. HBM-bound: (n_parts + 1)
+// rows*d elements moved.
+template <typename T>
+__global__ void __launch_bounds__(256) sum_partials_kernel(int n_parts, int64_t nvec,
+                                                           const T *__restrict__ partials,
+                                                           T *__restrict__ out) {
+  constexpr int N = Vec<T>::N;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+    float acc[N];
+    load16<T>(partials + v * N, acc);
+    for (int p = 1; p < n_parts; ++p) {
+      float y[N];
+      load16<T>(partials + ((int64_t)p * nvec + v) * N, y);
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = __fadd_rn(acc[i], y[i]);
+    }
+    store16<T>(out + v * N, acc);
+  }
+}
+
 // dx[t] = sum_k dXp[row_of[t,k]] (+ dx_add[t]), fp32, slot order.
 __global__ void __launch_bounds__(256)
 permute_bwd_kernel(int64_t T, int d, int K, const float *__restrict__ dXp,
@@ -399,6 +421,26 @@ cudaError_t launch_unpermute_bwd(const UnpermuteArgs &a, cudaStream_t s) {
     unpermute_bwd_kernel<__nv_bfloat16><<<(unsigned)a.T, 256, 0, s>>>(a);
   else
     unpermute_bwd_kernel<float><<<(unsigned)a.T, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum_partials(int dtype, int n_parts, int64_t rows, int d, const void *partials,
+                                void *out, cudaStream_t s) {
+  const int N = dtype == MOE_BF16 ? 8 : 4;
+  const int64_t nvec = rows * d / N;
+  if (nvec == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (nvec + 255) / 256, cap = (int64_t)(sms > 0 ? sms : 1) * 8;   // 8 CTAs per SM
+  const int64_t blocks = want < cap ? want : cap;
+  if (dtype == MOE_BF16)
+    sum_partials_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+        n_parts, nvec, reinterpret_cast<const __nv_bfloat16 *>(partials),
+        reinterpret_cast<__nv_bfloat16 *>(out));
+  else
+    sum_partials_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+        n_parts, nvec, reinterpret_cast<const float *>(partials), reinterpret_cast<float *>(out));
   return cudaGetLastError();
 }
 

@@ -24,10 +24,19 @@ def to_device(a: np.ndarray, device="cuda") -> torch.Tensor:
 
 class MoELayer:
     """One MoE layer of configuration `cfg` (a synthetic.MoEConfig-like object)
-    with device weights W_r, W_gu, W_down (+ b_r, w_sg, Ws_gu, Ws_down)."""
+    with device weights W_r, W_gu, W_down (+ b_r, w_sg, Ws_gu, Ws_down).
 
-    def __init__(self, cfg, weights: dict, device="cuda", backward=None):
+    etp > 1 runs the routed experts F-split the way an expert-tensor-parallel
+    group of `etp` ranks would (MoE Parallel Folding study notes, "method
+    overview": the expert's FFN dimension is sharded and a ReduceScatter-V
+    sums the partial outputs): shard s holds gate and up rows
+    [s*F/etp, (s+1)*F/etp) and the matching W_down columns, each shard is one
+    moe_expert_ffn call, and moe_sum_partials adds the partial Yp (and, in the
+    backward, the partial dXp) in shard order. Weight gradients stay per shard."""
+
+    def __init__(self, cfg, weights: dict, device="cuda", backward=None, etp: int = 1):
         self.cfg = cfg
+        self.etp = etp
         self.shape = L.shape_of(cfg)
         self.backward_enabled = cfg.backward if backward is None else backward
         self.w = weights
@@ -48,9 +57,21 @@ class MoELayer:
         self.src_of = z(N, dtype=torch.int32)
         self.counts = z(E, dtype=torch.int32)
         self.offsets = z(E + 1, dtype=torch.int32)
-        self.A_save = z(N, 2 * F) if self.backward_enabled else None
-        self.H = z(N, F)
+        self.A_save = z(N, 2 * F) if self.backward_enabled and etp == 1 else None
+        self.H = z(N, F) if etp == 1 else None
         self.Yp = z(N, d)
+        if etp > 1:
+            if F % etp != 0:
+                raise ValueError(f"F={F} does not split into {etp} shards")
+            Fl = F // etp
+            self.Fl = Fl
+            Wgu, Wdn = weights["W_gu"], weights["W_down"]
+            self.W_gu_s = [torch.cat([Wgu[:, s * Fl:(s + 1) * Fl], Wgu[:, F + s * Fl:F + (s + 1) * Fl]],
+                                     dim=1).contiguous() for s in range(etp)]
+            self.W_down_s = [Wdn[:, :, s * Fl:(s + 1) * Fl].contiguous() for s in range(etp)]
+            self.A_s = [z(N, 2 * Fl) if self.backward_enabled else None for _ in range(etp)]
+            self.H_s = [z(N, Fl) for _ in range(etp)]
+            self.Y_parts = z(etp, N, d)
         self.out = z(T, d)
         self.shared = cfg.Fs > 0
         if self.shared:
@@ -65,10 +86,17 @@ class MoELayer:
         if self.backward_enabled:
             self.dYp = z(N, d)
             self.dw = z(T, K, dtype=torch.float32)
-            self.dA = z(N, 2 * F)
             self.dXp = z(N, d, dtype=torch.float32)
-            self.dW_gu = z(E, 2 * F, d, dtype=torch.float32)
-            self.dW_down = z(E, d, F, dtype=torch.float32)
+            if etp == 1:
+                self.dA = z(N, 2 * F)
+                self.dW_gu = z(E, 2 * F, d, dtype=torch.float32)
+                self.dW_down = z(E, d, F, dtype=torch.float32)
+            else:
+                Fl = self.Fl
+                self.dA_s = z(N, 2 * Fl)   # reused shard after shard
+                self.dX_parts = z(etp, N, d, dtype=torch.float32)
+                self.dW_gu = [z(E, 2 * Fl, d, dtype=torch.float32) for _ in range(etp)]
+                self.dW_down = [z(E, d, Fl, dtype=torch.float32) for _ in range(etp)]
             self.dW_r = z(E, d, dtype=torch.float32)
             self.db_r = z(E, dtype=torch.float32)
             self.dx_router = z(T, d, dtype=torch.float32)
@@ -90,14 +118,39 @@ class MoELayer:
                     self.topk_idx, self.topk_prob, self.topk_w, self.keep, self.ws, stream)
         L.moe_permute(s, x, self.topk_idx, self.keep, self.Xp, self.row_of, self.src_of,
                       self.counts, self.offsets, self.ws, stream)
-        L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.Xp,
-                         w["W_gu"], w["W_down"], self.A_save, self.H, self.Yp, self.ws, stream)
+        self.routed_ffn(stream)
         if self.shared:
             L.moe_expert_ffn(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, x, w["Ws_gu"],
                              w["Ws_down"], self.As, self.Hs, self.Ys, self.ws, stream)
         L.moe_unpermute(s, self.Yp, self.row_of, self.topk_w, self.Ys, self.gate_logit, self.out,
                         stream)
         return self.out
+
+    def routed_ffn(self, stream=None):
+        c, w = self.cfg, self.w
+        if self.etp == 1:
+            L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.Xp,
+                             w["W_gu"], w["W_down"], self.A_save, self.H, self.Yp, self.ws, stream)
+            return
+        for s in range(self.etp):
+            L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, self.Fl, c.E, self.offsets, self.Xp,
+                             self.W_gu_s[s], self.W_down_s[s], self.A_s[s], self.H_s[s],
+                             self.Y_parts[s], self.ws, stream)
+        L.moe_sum_partials(self.dtype_code, self.etp, c.T * c.K, c.d, self.Y_parts, self.Yp, stream)
+
+    def routed_ffn_bwd(self, stream=None):
+        c, w = self.cfg, self.w
+        if self.etp == 1:
+            L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.dYp,
+                                 self.Xp, self.A_save, self.H, w["W_gu"], w["W_down"], self.dA,
+                                 self.dXp, self.dW_gu, self.dW_down, self.ws, stream)
+            return
+        for s in range(self.etp):
+            L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, self.Fl, c.E, self.offsets,
+                                 self.dYp, self.Xp, self.A_s[s], self.H_s[s], self.W_gu_s[s],
+                                 self.W_down_s[s], self.dA_s, self.dX_parts[s], self.dW_gu[s],
+                                 self.dW_down[s], self.ws, stream)
+        L.moe_sum_partials(L.MOE_F32, self.etp, c.T * c.K, c.d, self.dX_parts, self.dXp, stream)
 
     def backward(self, dout: torch.Tensor, stream=None, ffn_events=None) -> dict:
         """ffn_events: optional (start, end) CUDA events recorded on the current
@@ -108,9 +161,7 @@ class MoELayer:
                             self.dz if self.shared else None, stream)
         if ffn_events is not None:
             ffn_events[0].record()
-        L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.dYp,
-                             self.Xp, self.A_save, self.H, w["W_gu"], w["W_down"], self.dA,
-                             self.dXp, self.dW_gu, self.dW_down, self.ws, stream)
+        self.routed_ffn_bwd(stream)
         if ffn_events is not None:
             ffn_events[1].record()
         dx_in = None
