@@ -224,6 +224,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", default="compact", choices=["compact", "padded"],
+                    help="permuted-row layout: compact (default) or the fixed [E, capacity] "
+                         "layout (token-dropping workloads)")
     ap.add_argument("--etp", type=int, default=1,
                     help="run the routed experts F-split into this many shards (the arithmetic "
                          "of an expert-tensor-parallel group, on one GPU)")
@@ -259,7 +262,7 @@ def main():
     cfg_r = dataclasses.replace(cfg, seed=cfg.seed + rank)   # each replica its own batch
     inp = make_inputs(cfg_r)
     w = {k: to_device(v) for k, v in inp.items() if k not in ("x", "dout")}
-    layer = MoELayer(cfg_r, w, etp=args.etp)
+    layer = MoELayer(cfg_r, w, etp=args.etp, layout=args.layout)
     x = to_device(inp["x"])
     layer.x = x   # the backward reads the forward's tokens
     dout = to_device(inp["dout"]) if cfg.backward else None
@@ -274,8 +277,9 @@ def main():
                     layer.topk_idx, layer.topk_prob, layer.topk_w, layer.keep, ws)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
         if record: e[0].record(stream)
-        L.moe_permute(s, x, layer.topk_idx, layer.keep, layer.Xp, layer.row_of, layer.src_of,
-                      layer.counts, layer.offsets, ws)
+        permute = L.moe_permute_padded if args.layout == "padded" else L.moe_permute
+        permute(s, x, layer.topk_idx, layer.keep, layer.Xp, layer.row_of, layer.src_of,
+                layer.counts, layer.offsets, ws)
         if record: e[1].record(stream)
         if record: e[2].record(stream)
         layer.routed_ffn()
@@ -319,7 +323,7 @@ def main():
     secs = t_start.elapsed_time(t_end) / 1e3
     agg = aggregate(cfg.T * args.steps, secs, world, dist)
 
-    n_kept = int(layer.offsets[-1].item())
+    n_kept = int(layer.counts.sum().item())   # kept rows (the padded layout computes more)
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
     perm_ms = statistics.mean(a.elapsed_time(b) for a, b in perm_ev)
     unperm_ms = statistics.mean(a.elapsed_time(b) for a, b in unperm_ev)
@@ -405,11 +409,13 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * agg["seconds"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic (seeded normal inputs, random-init weights)",
-            "config": dict(workload_config(cfg), **({"etp_shards": args.etp} if args.etp > 1 else {})),
+            "config": dict(workload_config(cfg), **({"etp_shards": args.etp} if args.etp > 1 else {}),
+                           **({"layout": "padded"} if args.layout == "padded" else {})),
             "clocks": clk,
             "e2e": {"value": e2e["value"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step(cfg, args.etp) * args.steps,
+            "gpu_launches": (launches_per_step(cfg, args.etp)
+                             + (1 if args.layout == "padded" else 0)) * args.steps,
             "roofline": {"kernel": "grouped SwiGLU GEMM (moe_expert_ffn: gate/up + down)",
                          "bound": "tensor", "achieved": achieved, "peak": bf16_peak,
                          "unit": "TFLOP/s", "frac": achieved / bf16_peak, "traffic": traffic,

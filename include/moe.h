@@ -137,6 +137,31 @@ moe_status_t moe_permute(const moe_shape_t *shape, const void *x,
                          int32_t *row_of, int32_t *src_of, int32_t *counts,
                          int32_t *offsets, void *ws, moe_stream_t stream);
 
+/* GShard-style fixed layout (the alternative to the compact one; token
+ * dropping only): expert e owns rows [e*C, (e+1)*C) of Xp, its kept rows
+ * first (token-ascending, as moe_permute orders them) and zero rows after.
+ * C = moe_padded_capacity(shape) = sum over sub-sequences of min(ceil(CF *
+ * S_j * K / E), S_j), the most rows the capacity rule can keep for one
+ * expert. MoE Parallel Folding study notes, "key modules" and "Q&A":
+ * capacity-factor dropping bounds every expert's tokens, which is what lets a
+ * dispatcher use fixed-size buffers.
+ * moe_padded_capacity returns 0 when shape->drop is 0, the shape is invalid,
+ * or E*C does not fit in int32.
+ *   out: Xp [E*C, d]; row_of [T,K] (-1 when dropped); src_of [E*C] (t*K+k of
+ *        each kept row, -1 on padding rows); counts [E]; offsets [E+1] =
+ *        {0, C, 2C, ..., E*C}, so moe_expert_ffn(max_rows = E*C, n_groups = E)
+ *        runs every padded row (zero rows give zero outputs) and
+ *        moe_unpermute / moe_unpermute_bwd / moe_permute_bwd read row_of as
+ *        for the compact layout.
+ * Errors: as moe_permute; MOE_ERR_UNSUPPORTED when shape->drop is 0; a kept
+ * count above C (keep not produced by the capacity rule) records
+ * MOE_ERR_DEVICE in the status word and leaves that slot dropped.           */
+int64_t moe_padded_capacity(const moe_shape_t *shape);
+moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x,
+                                const int32_t *topk_idx, const uint8_t *keep, void *Xp,
+                                int32_t *row_of, int32_t *src_of, int32_t *counts,
+                                int32_t *offsets, void *ws, moe_stream_t stream);
+
 /* Largest token count T that moe_permute_noalloc accepts. */
 #define MOE_PERMUTE_NOALLOC_MAX_TOKENS 131072
 

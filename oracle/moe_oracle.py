@@ -270,6 +270,46 @@ def build_map(idx: np.ndarray, keep: np.ndarray, E: int):
 # --------------------------------------------------------------------------
 # a5: permute  [notes/method]
 
+def padded_capacity(T: int, S: int, K: int, E: int, cf: float) -> int:
+    """Rows per expert of the GShard-style fixed layout: the most the
+    capacity rule can keep for one expert, summed over the sub-sequences;
+    an expert takes at most one slot per token, so min(cap_j, S_j)."""
+    S = S if 0 < S < T else T
+    return sum(min(capacity(cf, min(S, T - lo), K, E), min(S, T - lo)) for lo in range(0, T, S))
+
+
+def build_map_padded(idx: np.ndarray, keep: np.ndarray, E: int, C: int):
+    """Fixed [E, C] layout [notes/modules, Q&A: capacity bounds each expert's
+    tokens, so buffers can be fixed-size]: expert e owns rows [eC, (e+1)C),
+    its kept assignments first in token order, padding after.
+    Returns counts [E], offsets [E+1] = e*C, row_of [T,K] (-1 dropped),
+    src_of [E*C] (-1 on padding rows)."""
+    T, K = idx.shape
+    counts = np.zeros(E, dtype=np.int32)
+    row_of = np.full((T, K), -1, dtype=np.int32)
+    src_of = np.full(E * C, -1, dtype=np.int32)
+    for t in range(T):
+        for k in range(K):
+            if keep[t, k]:
+                e = int(idx[t, k])
+                if counts[e] >= C:
+                    raise ValueError("more kept rows than the padded capacity")
+                row = e * C + int(counts[e])
+                row_of[t, k] = row
+                src_of[row] = t * K + k
+                counts[e] += 1
+    offsets = (np.arange(E + 1) * C).astype(np.int32)
+    return counts, offsets, row_of, src_of
+
+
+def permute_padded(x: np.ndarray, src_of: np.ndarray, K: int) -> np.ndarray:
+    """Xp[row] = x[src_of[row] // K], zero on padding rows (src_of < 0)."""
+    Xp = np.zeros((src_of.shape[0],) + x.shape[1:], dtype=x.dtype)
+    m = src_of >= 0
+    Xp[m] = x[src_of[m] // K]
+    return Xp
+
+
 def permute(x: np.ndarray, src_of: np.ndarray, K: int) -> np.ndarray:
     """Xp[row] = x[src_of[row] // K] (an exact copy; same dtype as x)."""
     return x[src_of // K]

@@ -143,3 +143,42 @@ def test_map_invariants(drop):
         seg = slice(offsets[e], offsets[e + 1])
         assert np.all(e_of[seg] == e)
         assert np.all(np.diff(t_of[seg]) > 0)
+
+
+# ---- GShard-style padded layout (f2) ----
+
+def test_padded_map_is_the_compact_map_with_fixed_strides():
+    """Expert e's rows of the padded map are its compact rows shifted from
+    offsets[e] to e*C, in the same order; padding rows are empty; every kept
+    expert count fits the capacity the drop rule implies."""
+    rng = np.random.default_rng(3)
+    for T, S, E, K, cf in [(60, 16, 4, 2, 1.0), (45, 45, 8, 3, 0.75), (33, 8, 5, 2, 4.0)]:
+        logits = rng.standard_normal((T, E))
+        p = O.softmax_f32(logits)
+        idx, prob = O.topk(p, K)
+        keep = O.capacity_keep(idx, prob, E, cf, S)
+        C = O.padded_capacity(T, S, K, E, cf)
+        counts, offsets, row_of, src_of, n = O.build_map(idx, keep, E)
+        pc, po, prow, psrc = O.build_map_padded(idx, keep, E, C)
+        assert np.array_equal(pc, counts) and counts.max() <= C
+        assert np.array_equal(po, np.arange(E + 1) * C)
+        for e in range(E):
+            assert np.array_equal(psrc[e * C:e * C + counts[e]], src_of[offsets[e]:offsets[e + 1]])
+            assert np.all(psrc[e * C + counts[e]:(e + 1) * C] == -1)
+        kept = keep.astype(bool)
+        e_of = idx.astype(np.int64)
+        assert np.array_equal(prow[kept] - e_of[kept] * C, row_of[kept] - offsets[e_of[kept]])
+        assert np.all(prow[~kept] == -1)
+        x = rng.standard_normal((T, 6)).astype(np.float32)
+        Xp = O.permute_padded(x, psrc, K)
+        assert np.array_equal(Xp[psrc >= 0], x[psrc[psrc >= 0] // K])
+        assert not Xp[psrc < 0].any()
+
+
+def test_padded_capacity_formula():
+    # two sub-sequences of 4096, cap = ceil(1.0 * 4096 * 2 / 8) = 1024 each
+    assert O.padded_capacity(8192, 4096, 2, 8, 1.0) == 2048
+    # full sequence: S = 0 means S = T
+    assert O.padded_capacity(100, 0, 2, 4, 1.0) == 50
+    # capacity above the sub-sequence length is clipped to it (one slot per token)
+    assert O.padded_capacity(10, 4, 2, 2, 4.0) == 4 + 4 + 2

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_route_topk": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute_noalloc": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_permute_padded": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_expert_ffn": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -71,11 +72,14 @@ for _name, _args in _SIGS.items():
     _f.restype = ctypes.c_int
 lib.moe_workspace_size.argtypes = [_S]
 lib.moe_workspace_size.restype = ctypes.c_size_t
+lib.moe_padded_capacity.argtypes = [_S]
+lib.moe_padded_capacity.restype = ctypes.c_int64
 lib.moe_version.restype = ctypes.c_char_p
 lib.moe_status_string.argtypes = [ctypes.c_int]
 lib.moe_status_string.restype = ctypes.c_char_p
 
-EXPORTED = sorted(list(_SIGS) + ["moe_workspace_size", "moe_version", "moe_status_string"])
+EXPORTED = sorted(list(_SIGS) + ["moe_workspace_size", "moe_version", "moe_status_string",
+                                  "moe_padded_capacity"])
 
 
 def _ptr(t):
@@ -134,6 +138,17 @@ def moe_route_topk(shape, logits, topk_idx, topk_prob, topk_w, keep, ws, stream=
 def moe_permute(shape, x, topk_idx, keep, Xp, row_of, src_of, counts, offsets, ws, stream=None):
     _call("moe_permute", ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(keep), _ptr(Xp),
           _ptr(row_of), _ptr(src_of), _ptr(counts), _ptr(offsets), _ptr(ws), _stream(stream))
+
+
+def moe_padded_capacity(shape: MoEShape) -> int:
+    return int(lib.moe_padded_capacity(ctypes.byref(shape)))
+
+
+def moe_permute_padded(shape, x, topk_idx, keep, Xp, row_of, src_of, counts, offsets, ws,
+                       stream=None):
+    _call("moe_permute_padded", ctypes.byref(shape), _ptr(x), _ptr(topk_idx), _ptr(keep),
+          _ptr(Xp), _ptr(row_of), _ptr(src_of), _ptr(counts), _ptr(offsets), _ptr(ws),
+          _stream(stream))
 
 
 def moe_permute_noalloc(shape, x, topk_idx, keep, Xp, row_of, src_of, counts, offsets,

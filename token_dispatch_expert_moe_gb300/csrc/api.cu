@@ -159,6 +159,34 @@ moe_status_t moe_permute(const moe_shape_t *shape, const void *x, const int32_t 
   return cuda_status(launch_permute(a, (cudaStream_t)stream));
 }
 
+int64_t moe_padded_capacity(const moe_shape_t *shape) {
+  if (!shape_ok(shape) || !shape->drop) return 0;
+  const int64_t C = padded_rows_per_expert(shape->T, subseq(shape), shape->K, shape->E,
+                                           shape->capacity_factor);
+  return C * shape->E < (int64_t(1) << 31) ? C : 0;
+}
+
+moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
+                                const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
+                                int32_t *counts, int32_t *offsets, void *ws, moe_stream_t stream) {
+  if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
+  if (!shape->drop) return MOE_ERR_UNSUPPORTED;   // dropless routing has no fixed capacity
+  if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets || !ws)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Xp) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const int64_t C = moe_padded_capacity(shape);
+  if (C <= 0) return MOE_ERR_UNSUPPORTED;
+  PermuteArgs a{};
+  a.T = shape->T; a.d = shape->d; a.E = shape->E; a.K = shape->K; a.dtype = shape->dtype;
+  a.x = x; a.topk_idx = topk_idx; a.keep = keep; a.Xp = Xp; a.row_of = row_of; a.src_of = src_of;
+  a.counts = counts; a.offsets = offsets; a.pad_rows = C;
+  a.blk_counts = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + layout(shape).map);
+  a.status = status_word(ws);
+  cudaError_t e = launch_permute(a, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = launch_pad_fill(a, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
 moe_status_t moe_permute_noalloc(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
                                  const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
                                  int32_t *counts, int32_t *offsets, moe_stream_t stream) {

@@ -29,6 +29,7 @@ enum : uint32_t {
   kInfoRowRange = 0x100,      // a permuted row index outside [0, max_rows)
   kInfoExpertRange = 0x200,   // an expert index outside [0, E)
   kInfoOffsets = 0x300,       // offsets not monotone or beyond max_rows
+  kInfoPadOverflow = 0x400,   // padded layout: more kept rows for an expert than its capacity
   kInfoGemmTimeout = 0x1000,  // + role: a GEMM pipeline wait gave up
 };
 
@@ -145,8 +146,13 @@ struct PermuteArgs {
   int32_t *row_of, *src_of, *counts, *offsets;
   int32_t *blk_counts;  // ws region [nblk, E]
   uint32_t *status;
+  int64_t pad_rows;     // 0: compact layout; > 0: expert e owns rows [e*pad_rows, (e+1)*pad_rows)
 };
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s);
+cudaError_t launch_pad_fill(const PermuteArgs &a, cudaStream_t s);
+// Rows per expert of the padded layout: sum over sub-sequences of
+// min(capacity, sub-sequence length) (an expert takes at most one slot per token).
+int64_t padded_rows_per_expert(int64_t T, int64_t S, int K, int E, float cf);
 cudaError_t launch_permute_noalloc(PermuteArgs a, cudaStream_t s);
 
 struct UnpermuteArgs {

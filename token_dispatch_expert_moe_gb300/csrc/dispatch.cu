@@ -75,12 +75,16 @@ __global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a, i
   if (threadIdx.x < E) {
     const int e = threadIdx.x;
     int off = 0;
-    for (int i = 0; i < e; ++i) off += tot_s[i];
+    if (a.pad_rows > 0) {   // padded layout: fixed stride per expert
+      off = (int)(e * a.pad_rows);
+    } else {
+      for (int i = 0; i < e; ++i) off += tot_s[i];
+    }
     base_s[e] += off;
     if (blockIdx.x == 0) {
       a.counts[e] = tot_s[e];
       a.offsets[e] = off;
-      if (e == E - 1) a.offsets[E] = off + tot_s[e];
+      if (e == E - 1) a.offsets[E] = a.pad_rows > 0 ? (int)(E * a.pad_rows) : off + tot_s[e];
     }
   }
   __syncthreads();
@@ -102,7 +106,12 @@ __global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a, i
         int rank = __popc(bm[e * 8 + wi] & below);
         for (int w = 0; w < wi; ++w) rank += __popc(bm[e * 8 + w]);
         row = base_s[e] + rank;
-        a.src_of[row] = (int32_t)(t * K + k);
+        if (a.pad_rows > 0 && row - e * a.pad_rows >= a.pad_rows) {
+          report(a.status, MOE_ERR_DEVICE, kInfoPadOverflow);
+          row = -1;
+        } else {
+          a.src_of[row] = (int32_t)(t * K + k);
+        }
       }
       a.row_of[t * K + k] = row;
     }
@@ -171,6 +180,17 @@ __global__ void __launch_bounds__(32) permute_bulk_kernel(PermuteArgs a, uint32_
   }
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Padded layout: rows [e*pad + counts[e], (e+1)*pad) of every expert get zero
+// activations and src_of = -1. One CTA per expert, 16-byte stores.
+__global__ void __launch_bounds__(256) pad_fill_kernel(PermuteArgs a, int vec_per_row) {
+  const int e = blockIdx.x;
+  const int64_t lo = (int64_t)e * a.pad_rows + a.counts[e], hi = (int64_t)(e + 1) * a.pad_rows;
+  uint4 *Xp = static_cast<uint4 *>(a.Xp);
+  for (int64_t i = lo * vec_per_row + threadIdx.x; i < hi * vec_per_row; i += blockDim.x)
+    Xp[i] = make_uint4(0, 0, 0, 0);
+  for (int64_t r = lo + threadIdx.x; r < hi; r += blockDim.x) a.src_of[r] = -1;
 }
 
 // out[t] = sum_k w[t,k] Yp[row_of[t,k]] (+ sigmoid(z_t) Ys[t]), fp32 sum in
@@ -421,6 +441,12 @@ cudaError_t launch_unpermute_bwd(const UnpermuteArgs &a, cudaStream_t s) {
     unpermute_bwd_kernel<__nv_bfloat16><<<(unsigned)a.T, 256, 0, s>>>(a);
   else
     unpermute_bwd_kernel<float><<<(unsigned)a.T, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_fill(const PermuteArgs &a, cudaStream_t s) {
+  const int vec_per_row = a.d * (a.dtype == MOE_BF16 ? 2 : 4) / 16;
+  pad_fill_kernel<<<(unsigned)a.E, 256, 0, s>>>(a, vec_per_row);
   return cudaGetLastError();
 }
 

@@ -230,6 +230,16 @@ cudaError_t launch_topk_from_logits(const RouteArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+int64_t padded_rows_per_expert(int64_t T, int64_t S, int K, int E, float cf) {
+  int64_t rows = 0;
+  for (int64_t lo = 0; lo < T; lo += S) {
+    const int64_t len = T - lo < S ? T - lo : S;
+    const int64_t cap = capacity_of(cf, len, K, E);
+    rows += cap < len ? cap : len;
+  }
+  return rows;
+}
+
 cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s) {
   const int64_t n_sub = (a.T + a.S - 1) / a.S;
   const int64_t last = a.T - (n_sub - 1) * a.S;

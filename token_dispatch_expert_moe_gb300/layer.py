@@ -32,11 +32,17 @@ class MoELayer:
     sums the partial outputs): shard s holds gate and up rows
     [s*F/etp, (s+1)*F/etp) and the matching W_down columns, each shard is one
     moe_expert_ffn call, and moe_sum_partials adds the partial Yp (and, in the
-    backward, the partial dXp) in shard order. Weight gradients stay per shard."""
+    backward, the partial dXp) in shard order. Weight gradients stay per shard.
 
-    def __init__(self, cfg, weights: dict, device="cuda", backward=None, etp: int = 1):
+    layout="padded" (token dropping only) uses the fixed GShard-style layout of
+    moe_permute_padded: expert e owns rows [e*C, (e+1)*C), zero rows after its
+    kept ones, and the grouped GEMMs run every padded row."""
+
+    def __init__(self, cfg, weights: dict, device="cuda", backward=None, etp: int = 1,
+                 layout: str = "compact"):
         self.cfg = cfg
         self.etp = etp
+        self.layout = layout
         self.shape = L.shape_of(cfg)
         self.backward_enabled = cfg.backward if backward is None else backward
         self.w = weights
@@ -44,7 +50,16 @@ class MoELayer:
         dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
         self.dt = dt
         self.dtype_code = L.MOE_BF16 if cfg.dtype == "bf16" else L.MOE_F32
-        N = T * K
+        if layout == "padded":
+            C = L.moe_padded_capacity(L.shape_of(cfg))
+            if C <= 0:
+                raise ValueError("the padded layout needs token dropping (a fixed capacity)")
+            N = E * C
+        elif layout == "compact":
+            N = T * K
+        else:
+            raise ValueError(f"unknown layout {layout!r}")
+        self.rows = N   # rows of the permuted buffers
         z = lambda *s, dtype=dt: torch.empty(*s, dtype=dtype, device=device)  # noqa: E731
         self.ws = torch.zeros(L.moe_workspace_size(self.shape), dtype=torch.uint8, device=device)
         self.logits = z(T, E, dtype=torch.float32)
@@ -84,7 +99,9 @@ class MoELayer:
         else:
             self.gate_logit = self.Ys = None
         if self.backward_enabled:
-            self.dYp = z(N, d)
+            # zeros: in the padded layout the padding rows of dYp are never
+            # written, and the weight gradients read them (times zero activations)
+            self.dYp = torch.zeros((N, d), dtype=dt, device=device)
             self.dw = z(T, K, dtype=torch.float32)
             self.dXp = z(N, d, dtype=torch.float32)
             if etp == 1:
@@ -116,8 +133,9 @@ class MoELayer:
         self.x = x
         L.moe_route(s, x, w["W_r"], w.get("b_r"), w.get("w_sg"), self.logits, self.gate_logit,
                     self.topk_idx, self.topk_prob, self.topk_w, self.keep, self.ws, stream)
-        L.moe_permute(s, x, self.topk_idx, self.keep, self.Xp, self.row_of, self.src_of,
-                      self.counts, self.offsets, self.ws, stream)
+        permute = L.moe_permute_padded if self.layout == "padded" else L.moe_permute
+        permute(s, x, self.topk_idx, self.keep, self.Xp, self.row_of, self.src_of,
+                self.counts, self.offsets, self.ws, stream)
         self.routed_ffn(stream)
         if self.shared:
             L.moe_expert_ffn(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, x, w["Ws_gu"],
@@ -129,28 +147,28 @@ class MoELayer:
     def routed_ffn(self, stream=None):
         c, w = self.cfg, self.w
         if self.etp == 1:
-            L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.Xp,
+            L.moe_expert_ffn(self.dtype_code, self.rows, c.d, c.F, c.E, self.offsets, self.Xp,
                              w["W_gu"], w["W_down"], self.A_save, self.H, self.Yp, self.ws, stream)
             return
         for s in range(self.etp):
-            L.moe_expert_ffn(self.dtype_code, c.T * c.K, c.d, self.Fl, c.E, self.offsets, self.Xp,
+            L.moe_expert_ffn(self.dtype_code, self.rows, c.d, self.Fl, c.E, self.offsets, self.Xp,
                              self.W_gu_s[s], self.W_down_s[s], self.A_s[s], self.H_s[s],
                              self.Y_parts[s], self.ws, stream)
-        L.moe_sum_partials(self.dtype_code, self.etp, c.T * c.K, c.d, self.Y_parts, self.Yp, stream)
+        L.moe_sum_partials(self.dtype_code, self.etp, self.rows, c.d, self.Y_parts, self.Yp, stream)
 
     def routed_ffn_bwd(self, stream=None):
         c, w = self.cfg, self.w
         if self.etp == 1:
-            L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, c.F, c.E, self.offsets, self.dYp,
+            L.moe_expert_ffn_bwd(self.dtype_code, self.rows, c.d, c.F, c.E, self.offsets, self.dYp,
                                  self.Xp, self.A_save, self.H, w["W_gu"], w["W_down"], self.dA,
                                  self.dXp, self.dW_gu, self.dW_down, self.ws, stream)
             return
         for s in range(self.etp):
-            L.moe_expert_ffn_bwd(self.dtype_code, c.T * c.K, c.d, self.Fl, c.E, self.offsets,
+            L.moe_expert_ffn_bwd(self.dtype_code, self.rows, c.d, self.Fl, c.E, self.offsets,
                                  self.dYp, self.Xp, self.A_s[s], self.H_s[s], self.W_gu_s[s],
                                  self.W_down_s[s], self.dA_s, self.dX_parts[s], self.dW_gu[s],
                                  self.dW_down[s], self.ws, stream)
-        L.moe_sum_partials(L.MOE_F32, self.etp, c.T * c.K, c.d, self.dX_parts, self.dXp, stream)
+        L.moe_sum_partials(L.MOE_F32, self.etp, self.rows, c.d, self.dX_parts, self.dXp, stream)
 
     def backward(self, dout: torch.Tensor, stream=None, ffn_events=None) -> dict:
         """ffn_events: optional (start, end) CUDA events recorded on the current
