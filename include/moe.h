@@ -233,6 +233,11 @@ moe_status_t moe_unpermute_bwd(const moe_shape_t *shape, const void *dout,
                                const float *gate_logit, void *dYp, float *dw,
                                void *dYs, float *dz, moe_stream_t stream);
 
+/* Workspace bytes moe_expert_ffn_bwd needs: the status word and, for bf16,
+ * the weight-gradient GEMMs' per-group tensor maps. moe_workspace_size()
+ * never returns less than this for a valid shape.                           */
+#define MOE_FFN_BWD_WORKSPACE_BYTES 33280u
+
 /* Backward of moe_expert_ffn (same argument meanings).
  *   in:  dYp [max_rows,d] dtype; Xp; A_save; H_save; W_gu; W_down.
  *   out: dXp [max_rows, d] fp32 = dA W_gu; dW_gu [n_groups,2F,d] fp32 =
@@ -240,13 +245,15 @@ moe_status_t moe_unpermute_bwd(const moe_shape_t *shape, const void *dout,
  *        with no rows);
  *   dA [max_rows, 2F] dtype: caller-owned buffer that receives
  *   [dG | dU] = [dH*U*sg*(1+G(1-sg)) | dH*G*sg], dH = dYp W_down,
- *   sg = sigmoid(G), G|U from A_save.                                        */
+ *   sg = sigmoid(G), G|U from A_save.
+ *   ws: ws_bytes bytes, 16-byte aligned; ws_bytes below
+ *   MOE_FFN_BWD_WORKSPACE_BYTES returns MOE_ERR_INVALID_ARG.                 */
 moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int32_t F,
                                 int32_t n_groups, const int32_t *offsets,
                                 const void *dYp, const void *Xp, const void *A_save,
                                 const void *H_save, const void *W_gu,
                                 const void *W_down, void *dA, float *dXp,
-                                float *dW_gu, float *dW_down, void *ws,
+                                float *dW_gu, float *dW_down, void *ws, size_t ws_bytes,
                                 moe_stream_t stream);
 
 /* dx[t] = sum over kept slots of dXp[row_of[t,k]] (+ dx_add[t]), fp32.

@@ -95,3 +95,7 @@ def test_invalid_arguments_rejected_on_host(L):
             L.moe_sum_partials(*args, 0)
         assert e.value.code == 1, args
     L.moe_sum_partials(1, 2, 0, 64, None, None, 0)   # zero rows: nothing to do
+    with pytest.raises(L.MoEError) as e:   # ffn backward: workspace too small for the group maps
+        L.moe_expert_ffn_bwd(1, 32, 128, 128, 4, fake, fake, fake, fake, fake, fake, fake, fake,
+                             fake, fake, fake, fake, 0, ws_bytes=L.MOE_FFN_BWD_WORKSPACE_BYTES - 256)
+    assert e.value.code == 1

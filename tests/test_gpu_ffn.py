@@ -97,7 +97,7 @@ def _check_bwd(L, dtype, Xp, offsets, W_gu, W_down, dYp, d, F):
     dX = empty((n, d), torch.float32)
     dWgu = empty((G, 2 * F, d), torch.float32)
     dWd = empty((G, d, F), torch.float32)
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(L.MOE_FFN_BWD_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
     L.moe_expert_ffn_bwd(code, n, d, F, G, dev(offsets), dY, dev(Xp), A, H, dev(W_gu), dev(W_down),
                          dA, dX, dWgu, dWd, ws)
     rc, info = L.moe_get_status(ws)

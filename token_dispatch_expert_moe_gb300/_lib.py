@@ -15,6 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_FFN_BWD_WORKSPACE_BYTES = 33280   # include/moe.h
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
           4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE"}
 
@@ -59,7 +60,7 @@ _SIGS = {
     "moe_unpermute": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_expert_ffn_bwd": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                           _P, _P, _P, _P],
+                           _P, _P, _P, ctypes.c_size_t, _P],
     "moe_permute_bwd": [_S, _P, _P, _P, _P, _P],
     "moe_sum_partials": [_I32, _I32, _I64, _I32, _P, _P, _P],
     "moe_route_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -177,10 +178,13 @@ def moe_unpermute_bwd(shape, dout, Yp, row_of, topk_w, Ys, gate_logit, dYp, dw, 
 
 
 def moe_expert_ffn_bwd(dtype, max_rows, d, F, n_groups, offsets, dYp, Xp, A_save, H_save, W_gu,
-                       W_down, dA, dXp, dW_gu, dW_down, ws, stream=None):
+                       W_down, dA, dXp, dW_gu, dW_down, ws, stream=None, ws_bytes=None):
+    """ws: a device tensor (its size becomes ws_bytes) or a pointer with ws_bytes."""
+    if ws_bytes is None:
+        ws_bytes = ws.numel() * ws.element_size()
     _call("moe_expert_ffn_bwd", dtype, max_rows, d, F, n_groups, _ptr(offsets), _ptr(dYp),
           _ptr(Xp), _ptr(A_save), _ptr(H_save), _ptr(W_gu), _ptr(W_down), _ptr(dA), _ptr(dXp),
-          _ptr(dW_gu), _ptr(dW_down), _ptr(ws), _stream(stream))
+          _ptr(dW_gu), _ptr(dW_down), _ptr(ws), ws_bytes, _stream(stream))
 
 
 def moe_permute_bwd(shape, dXp, row_of, dx_add, dx, stream=None):

@@ -48,7 +48,7 @@ Layout layout(const moe_shape_t *s) {
   }
   L.rbwd = off;
   off += align256(route_bwd_workspace_bytes(s->T, s->d, s->E));
-  L.total = off;
+  L.total = off > MOE_FFN_BWD_WORKSPACE_BYTES ? off : MOE_FFN_BWD_WORKSPACE_BYTES;
   return L;
 }
 
@@ -266,9 +266,11 @@ moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int3
                                 int32_t n_groups, const int32_t *offsets, const void *dYp,
                                 const void *Xp, const void *A_save, const void *H_save,
                                 const void *W_gu, const void *W_down, void *dA, float *dXp,
-                                float *dW_gu, float *dW_down, void *ws, moe_stream_t stream) {
+                                float *dW_gu, float *dW_down, void *ws, size_t ws_bytes,
+                                moe_stream_t stream) {
   moe_status_t st = ffn_check(dtype, max_rows, d, F, n_groups, offsets, ws);
   if (st != MOE_OK) return st;
+  if (ws_bytes < MOE_FFN_BWD_WORKSPACE_BYTES) return MOE_ERR_INVALID_ARG;
   if (!dYp || !Xp || !A_save || !H_save || !W_gu || !W_down || !dA || !dXp || !dW_gu || !dW_down)
     return MOE_ERR_INVALID_ARG;
   const void *ptrs[] = {dYp, Xp, A_save, H_save, W_gu, W_down, dA, dXp, dW_gu, dW_down};
@@ -279,6 +281,11 @@ moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int3
   a.offsets = offsets; a.dYp = dYp; a.Xp = Xp; a.A_save = const_cast<void *>(A_save);
   a.H_save = const_cast<void *>(H_save); a.W_gu = W_gu; a.W_down = W_down; a.dA = dA;
   a.dXp = dXp; a.dW_gu = dW_gu; a.dW_down = dW_down; a.status = status_word(ws);
+  // group tensor maps after the status word, 128-byte aligned
+  a.maps = reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(ws) + kStatusBytes + 127) &
+                                    ~uintptr_t(127));
+  static_assert(kStatusBytes + 127 + kFfnMapBytes <= MOE_FFN_BWD_WORKSPACE_BYTES,
+                "group maps exceed the documented workspace");
   cudaStream_t s = (cudaStream_t)stream;
   return cuda_status(dtype == MOE_BF16 ? launch_ffn_bwd_bf16(a, s) : launch_ffn_bwd_f32(a, s));
 }

@@ -184,8 +184,14 @@ struct FfnArgs {
   void *dA;
   float *dXp, *dW_gu, *dW_down;
   void *H_tmp;  // fwd scratch for H when H_save is NULL (ws)
+  void *maps;   // bwd (bf16): kFfnMapBytes of workspace, 128-byte aligned, for group tensor maps
   uint32_t *status;
 };
+// Group tensor maps of the bf16 weight-gradient GEMMs: 2 modes x 2 maps x 64
+// groups x 128 bytes, after the 256-byte status word (rounded to 128 bytes).
+constexpr int kMaxMapGroups = 64;
+constexpr size_t kFfnMapBytes = 2 * 2 * kMaxMapGroups * 128;
+constexpr size_t kFfnBwdWorkspaceBytes = 256 + 128 + kFfnMapBytes;
 size_t ffn_workspace_bytes(int dtype, int64_t max_rows, int d, int F);
 cudaError_t launch_ffn_fwd_f32(const FfnArgs &a, cudaStream_t s);
 cudaError_t launch_ffn_bwd_f32(const FfnArgs &a, cudaStream_t s);

@@ -52,7 +52,6 @@ constexpr int kStages = 4;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
-constexpr int kPairThreads = 224;  // + warp 6: zeroes ragged K blocks (weight-gradient modes)
 constexpr int kABytes = BM * BK * 2;          // 16 KB
 constexpr int kBBytesMax = 256 * BK * 2;      // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
@@ -79,6 +78,10 @@ struct TcParams {
   void *out0;    // GU: H; DOWN: Yp; DH: dA; DX: dXp; WG*: dW
   void *out1;    // GU: A_save (nullable)
   const void *aux;  // DH: A_save
+  // WGD/WGU: per group, the A and B tensor maps of that group's rows alone
+  // ([2g] = A, [2g+1] = B; outer extent = the group's row count), so the TMA
+  // zero-fills the K rows past the group's end of a ragged last K block
+  const CUtensorMap *gmaps;
   int fault_stall;   // test hook: the producer issues no loads (waits run out)
   // RT
   int64_t T;
@@ -112,17 +115,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -137,6 +129,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+// Acquire side of a tensor map written by an earlier kernel (the group maps
+// of the weight-gradient modes): orders the map's bytes before its TMA use.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap *m) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(m) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -310,9 +307,6 @@ struct SharedState {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t ebar[4];  // DH: per-epilogue-warp A_save box loads
-  uint64_t zfull[kMaxStages];   // pair WG*: this CTA's own ragged-block loads
-  uint64_t zready[kMaxStages];  // pair WG*: odd CTA has zeroed its tail rows
-  uint64_t zdone[kMaxStages];   // pair WG*: even CTA's zeroing warp is done
   uint32_t tmem_base;
   volatile int abort;
   int total_tiles;
@@ -607,42 +601,6 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
   }
 }
 
-// bounded wait with cluster-scope acquire (signals that come from the peer CTA)
-__device__ bool wait_bounded_cluster(SharedState &st, uint32_t bar, uint32_t parity,
-                                     uint32_t *status, uint32_t role) {
-  const uint64_t t0 = globaltimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (st.abort) return false;
-    if (globaltimer() - t0 > kTimeoutNs) {
-      report(status, MOE_ERR_TIMEOUT, kInfoGemmTimeout + role);
-      st.abort = 1;
-      return false;
-    }
-  }
-}
-
-// Zero K rows [valid, 64) of a stage's boxes: A_BOXES boxes of A at sa,
-// B_BOXES boxes of B at sa + kABytes (MN-major boxes: 64 K rows x 128 B).
-template <int A_BOXES, int B_BOXES>
-__device__ __forceinline__ void zero_tail_rows(uint8_t *sa_p, int valid, int lane) {
-  // rows valid..BK-1 of every 64-row box are contiguous 128-byte lines, so
-  // each box's tail is one contiguous byte range (swizzling only permutes
-  // the 16-byte chunks inside a line)
-  const int nchunks = (BK - valid) * 8;
-#pragma unroll
-  for (int box = 0; box < A_BOXES + B_BOXES; ++box) {
-    uint8_t *tail = (box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192) +
-                    valid * 128;
-    for (int i = lane; i < nchunks; i += 32)
-      *reinterpret_cast<uint4 *>(tail + i * 16) = make_uint4(0, 0, 0, 0);
-  }
-  fence_proxy_async();
-  __syncwarp();
-}
-
 template <int MODE, int BN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using TR = ModeTraits<MODE>;
@@ -735,14 +693,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           last_phase[s] = (int)ph;
           const uint32_t sa = smem_u32(smem + s * kStageBytes);
           const uint32_t sb = sa + kABytes;
-          if constexpr (TR::red) {
-            const int krow = t.row0 + kb * BK;
+          if constexpr (TR::red) {   // K rows relative to the group's own maps
+            const CUtensorMap *mA = p.gmaps + 2 * t.g, *mB = mA + 1;
+            if (kb == 0) {
+              tensormap_acquire(mA);
+              tensormap_acquire(mB);
+            }
 #pragma unroll
             for (int b = 0; b < A_BOXES; ++b)
-              tma_load_2d(sa + b * 8192, &p.tmA, full, t.m * BM + 64 * b, krow);
+              tma_load_2d(sa + b * 8192, mA, full, t.m * BM + 64 * b, kb * BK);
 #pragma unroll
             for (int b = 0; b < B_BOXES; ++b)
-              tma_load_2d(sb + b * 8192, &p.tmB, full, t.n * BN + 64 * b, krow);
+              tma_load_2d(sb + b * 8192, mB, full, t.n * BN + 64 * b, kb * BK);
           } else {
             const int arow = t.row0 + t.m * BM;
             tma_load_2d(sa, &p.tmA, full, kb * BK, arow);
@@ -796,21 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         tc_fence_after();
         uint8_t *sa_p = smem + s * kStageBytes;
-        if constexpr (TR::red) {
-          const int valid = t.rows - kb * BK;
-          if (valid < BK) {
-            // zero K rows [valid, 64) of every box of A and B (128 B each)
-            const int nz = (BK - valid) * (A_BOXES + B_BOXES);
-            for (int i = lane; i < nz * 8; i += 32) {
-              const int line = i >> 3, chunk = i & 7;
-              const int box = line / (BK - valid), r = valid + line % (BK - valid);
-              uint8_t *base = box < A_BOXES ? sa_p + box * 8192 : sa_p + kABytes + (box - A_BOXES) * 8192;
-              *reinterpret_cast<uint4 *>(base + r * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async();
-          }
-          __syncwarp();
-        }
         if (lane == 0) {
           const uint32_t sa = smem_u32(sa_p);
           const uint32_t sb = sa + kABytes;
@@ -910,7 +857,7 @@ __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const Shared
 }
 
 template <int MODE, int BN>
-__global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
   using TR = ModeTraits<MODE>;
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
@@ -960,9 +907,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
     for (int i = 0; i < kPairStages; ++i) {
       mbar_init(smem_u32(&st.full[i]), 1);
       mbar_init(smem_u32(&st.empty[i]), 1);
-      mbar_init(smem_u32(&st.zfull[i]), 1);
-      mbar_init(smem_u32(&st.zready[i]), 1);
-      mbar_init(smem_u32(&st.zdone[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&st.tfull[b]), 1);
@@ -994,8 +938,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
       int last_phase[kPairStages];
 #pragma unroll
       for (int i = 0; i < kPairStages; ++i) last_phase[i] = -1;
-      uint32_t zuse = 0;    // bit s = parity of the next ragged use of stage s
-      uint32_t zlast = 0;   // bit s: stage s had a ragged use
       for (int pt = cid; pt < total && !st.abort; pt += ncl) {
         const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
         const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
@@ -1003,33 +945,26 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
           const int s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1;
           if (!wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 1)) break;
-          const bool ragged = TR::red && (t.rows - kb * BK < BK);
           const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
           const uint32_t sb = sa + kABytes;
-          // where this CTA's bytes complete: the even CTA's full barrier, or
-          // for a ragged block this CTA's own zfull barrier (its zeroing warp
-          // clears the tail rows after they land). full[s] still completes
-          // once per use of the stage: for a ragged block by a plain arrival.
-          uint32_t bar;
-          if (ragged) {
-            bar = map_to_cta(smem_u32(&st.zfull[s]), rank);
-            mbar_expect_tx(smem_u32(&st.zfull[s]), kOwnTx);
-            zuse ^= 1u << s;
-            zlast |= 1u << s;
-            if (leader) mbar_arrive(smem_u32(&st.full[s]));
-          } else {
-            bar = map_to_cta(smem_u32(&st.full[s]), 0);
-            if (leader) mbar_expect_tx(smem_u32(&st.full[s]), kTx);
+          // both CTAs' bytes complete on the even CTA's full barrier
+          const uint32_t bar = map_to_cta(smem_u32(&st.full[s]), 0);
+          if (leader) {
+            mbar_expect_tx(smem_u32(&st.full[s]), kTx);
+            last_phase[s] = (int)ph;
           }
-          if (leader) last_phase[s] = (int)ph;
-          if constexpr (TR::red) {
-            const int krow = t.row0 + kb * BK;
+          if constexpr (TR::red) {   // K rows relative to the group's own maps
+            const CUtensorMap *mA = p.gmaps + 2 * t.g, *mB = mA + 1;
+            if (kb == 0) {
+              tensormap_acquire(mA);
+              tensormap_acquire(mB);
+            }
 #pragma unroll
             for (int b = 0; b < A_BOXES; ++b)
-              tma_load_2d_pair(sa + b * 8192, &p.tmA, bar, t.m * BM + 64 * b, krow);
+              tma_load_2d_pair(sa + b * 8192, mA, bar, t.m * BM + 64 * b, kb * BK);
 #pragma unroll
             for (int b = 0; b < B_HALF_BOXES; ++b)
-              tma_load_2d_pair(sb + b * 8192, &p.tmB, bar, t.n * BN + (int)rank * HALF_N + 64 * b, krow);
+              tma_load_2d_pair(sb + b * 8192, mB, bar, t.n * BN + (int)rank * HALF_N + 64 * b, kb * BK);
           } else {
             tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
@@ -1046,20 +981,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
           }
         }
       }
-      // wait (bounded) for this CTA's copies still in flight: the even CTA's
-      // full barriers see the loads of both CTAs land; each CTA's zfull
-      // barriers see its own ragged blocks land
+      // wait (bounded) for the copies still in flight: the even CTA's full
+      // barriers see the loads of both CTAs land
       for (int i = 0; i < kPairStages; ++i) {
         if (leader && last_phase[i] >= 0) {
           const uint32_t b = smem_u32(&st.full[i]);
           const uint64_t t0 = globaltimer();
           while (!mbar_try_wait(b, (uint32_t)last_phase[i]) && globaltimer() - t0 < kTimeoutNs) {
-          }
-        }
-        if ((zlast >> i) & 1) {
-          const uint32_t b = smem_u32(&st.zfull[i]);
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(b, ((zuse >> i) & 1) ^ 1) && globaltimer() - t0 < kTimeoutNs) {
           }
         }
       }
@@ -1069,7 +997,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
       // ======================= MMA issuer (even CTA) =======================
       int it = 0, tcount = 0;
       bool issued_any = false;
-      uint32_t zuse = 0;   // bit s = parity of the next ragged use of stage s
       for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
         const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, 0);
         const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
@@ -1085,18 +1012,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
           if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
             ok = false;
             break;
-          }
-          if constexpr (TR::red) {
-            const int valid = t.rows - kb * BK;
-            if (valid < BK) {   // both CTAs' zeroing warps have cleared the tail rows
-              const uint32_t zp = (zuse >> s) & 1;
-              zuse ^= 1u << s;
-              if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.zdone[s]), zp, p.status, 8)) ||
-                  !__all_sync(0xffffffffu, wait_bounded_cluster(st, smem_u32(&st.zready[s]), zp, p.status, 6))) {
-                ok = false;
-                break;
-              }
-            }
           }
           tc_fence_after();
           if (lane == 0) {
@@ -1129,36 +1044,6 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
       }
       __syncwarp();
     }
-  } else if (warp == 6) {
-    // ===== both CTAs (weight-gradient modes): zero ragged K blocks' tail rows =====
-    // A ragged block's loads complete on this CTA's zfull[s], whose phases
-    // count the ragged uses of stage s only, so this warp waits for each of
-    // them in order. After zeroing: the even CTA signals its MMA warp through
-    // zdone[s], the odd CTA arrives on the even CTA's zready[s] (release,
-    // cluster scope).
-    if constexpr (TR::red) {
-      int it = 0;
-      uint32_t zuse = 0;
-      const uint32_t zready_leader0 = map_to_cta(smem_u32(&st.zready[0]), 0);
-      for (int pt = cid; pt < total && !st.abort; pt += ncl) {
-        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
-        const int kblocks = (t.rows + BK - 1) / BK;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int valid = t.rows - kb * BK;
-          if (valid >= BK) continue;
-          const int s = it % kPairStages;
-          const uint32_t zp = (zuse >> s) & 1;
-          zuse ^= 1u << s;
-          if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.zfull[s]), zp, p.status, 7))) break;
-          zero_tail_rows<A_BOXES, B_HALF_BOXES>(smem + s * kPairStageBytes, valid, lane);
-          if (lane == 0) {
-            if (leader) mbar_arrive(smem_u32(&st.zdone[s]));
-            else mbar_arrive_cluster(zready_leader0 + s * 8);
-          }
-          __syncwarp();
-        }
-      }
-    }
   } else {
     // ======================= epilogue (both CTAs) =======================
     const int q = warp & 3;
@@ -1190,6 +1075,41 @@ __global__ void __launch_bounds__(kPairThreads, 1) tc_gemm_pair_kernel(const __g
                  "r"(kTmemCols)
                  : "memory");
   }
+}
+
+// Group tensor maps of the weight-gradient modes: thread g copies the two
+// host-encoded templates (A and B over all rows) and points the copies at
+// group g's first row with an outer extent of the group's row count, so a K
+// block past the group's end is zero-filled by the TMA. An empty group gets
+// an extent of 1 (its tiles load nothing). Offsets outside [0, max_rows] are
+// reported by the GEMM kernel, which then loads nothing.
+__global__ void group_maps_kernel(const __grid_constant__ CUtensorMap tA,
+                                  const __grid_constant__ CUtensorMap tB, const int32_t *offsets,
+                                  int n_groups, const uint8_t *a_base, int64_t a_row_bytes,
+                                  const uint8_t *b_base, int64_t b_row_bytes, int64_t max_rows,
+                                  CUtensorMap *out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const int32_t lo = offsets[g], hi = offsets[g + 1];
+  const bool sane = lo >= 0 && hi >= lo && hi <= max_rows;
+  const int64_t row0 = sane ? lo : 0;
+  const uint32_t rows = sane && hi > lo ? (uint32_t)(hi - lo) : 1u;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(w == 0 ? &tA : &tB);
+    uint4 *dst = reinterpret_cast<uint4 *>(out + 2 * g + w);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(CUtensorMap) / sizeof(uint4)); ++i) dst[i] = src[i];
+    const uint64_t addr =
+        reinterpret_cast<uint64_t>(w == 0 ? a_base + row0 * a_row_bytes : b_base + row0 * b_row_bytes);
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(dst),
+                 "l"(addr)
+                 : "memory");
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst),
+                 "r"(rows)
+                 : "memory");
+  }
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -1281,7 +1201,7 @@ cudaError_t launch_pair(TcParams p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
-  cfg.blockDim = dim3(kPairThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1390,20 +1310,34 @@ cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
     if (!make_store_map(&q.tmO0, a.dXp, 4, d, a.max_rows)) return cudaErrorInvalidValue;
     if ((e = launch_bn<DX>(q, s)) != cudaSuccess) return e;
   }
+  // the weight-gradient GEMMs read per-group tensor maps (two regions of the
+  // workspace, one per mode, 2 * n_groups maps each)
+  CUtensorMap *maps = static_cast<CUtensorMap *>(a.maps);
   {  // WGD: dW_down[g] = dYp_g^T H_g
     TcParams q = p;
     if (!make_map(&q.tmA, a.dYp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.H_save, F, a.max_rows, 64)) return cudaErrorInvalidValue;
-    q.mode = WGD; q.M_fixed = d; q.N = F; q.out0 = a.dW_down;
+    q.mode = WGD; q.M_fixed = d; q.N = F; q.out0 = a.dW_down; q.gmaps = maps;
     if (!make_store_map(&q.tmO0, a.dW_down, 4, F, (uint64_t)E * d)) return cudaErrorInvalidValue;
+    group_maps_kernel<<<1, 64, 0, s>>>(q.tmA, q.tmB, a.offsets, E,
+                                       static_cast<const uint8_t *>(a.dYp), 2 * (int64_t)d,
+                                       static_cast<const uint8_t *>(a.H_save), 2 * (int64_t)F,
+                                       a.max_rows, maps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_bn<WGD>(q, s)) != cudaSuccess) return e;
   }
   {  // WGU: dW_gu[g] = dA_g^T Xp_g
     TcParams q = p;
     if (!make_map(&q.tmA, a.dA, 2 * F, a.max_rows, 64)) return cudaErrorInvalidValue;
     if (!make_map(&q.tmB, a.Xp, d, a.max_rows, 64)) return cudaErrorInvalidValue;
-    q.mode = WGU; q.M_fixed = 2 * F; q.N = d; q.out0 = a.dW_gu;
+    CUtensorMap *maps_u = maps + 2 * kMaxMapGroups;
+    q.mode = WGU; q.M_fixed = 2 * F; q.N = d; q.out0 = a.dW_gu; q.gmaps = maps_u;
     if (!make_store_map(&q.tmO0, a.dW_gu, 4, d, (uint64_t)E * 2 * F)) return cudaErrorInvalidValue;
+    group_maps_kernel<<<1, 64, 0, s>>>(q.tmA, q.tmB, a.offsets, E,
+                                       static_cast<const uint8_t *>(a.dA), 4 * (int64_t)F,
+                                       static_cast<const uint8_t *>(a.Xp), 2 * (int64_t)d,
+                                       a.max_rows, maps_u);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = launch_bn<WGU>(q, s)) != cudaSuccess) return e;
   }
   return cudaSuccess;
