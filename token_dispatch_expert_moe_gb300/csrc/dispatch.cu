@@ -26,8 +26,18 @@ namespace {
 
 constexpr int kMapBlock = 256;  // tokens per map CTA (8 words of 32 bits)
 
+// Programmatic dependent launch: the map scatter and the row copy are
+// launched while their predecessor still runs; each waits for it (and its
+// memory) at griddepcontrol.wait before reading what it wrote. Inputs written
+// before the whole call (x, topk_idx, keep) may be read before the wait.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kMapBlock) map_count_kernel(PermuteArgs a) {
   extern __shared__ uint32_t bm[];  // [E][8]
+  pdl_trigger();
   const int E = a.E, K = a.K;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0;
   __syncthreads();
@@ -56,8 +66,10 @@ __global__ void __launch_bounds__(kMapBlock) map_count_kernel(PermuteArgs a) {
 __global__ void __launch_bounds__(kMapBlock) map_scatter_kernel(PermuteArgs a, int nblk) {
   extern __shared__ uint32_t bm[];  // [E][8]
   __shared__ int tot_s[64], base_s[64];
+  pdl_trigger();
   const int E = a.E, K = a.K;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0;
+  pdl_wait();   // blk_counts come from map_count
   // every CTA scans the (small) table of per-block counts itself: expert
   // totals, and the kept assignments of expert e in blocks before this one
   if (threadIdx.x < E) {
@@ -152,6 +164,7 @@ __global__ void __launch_bounds__(32) permute_bulk_kernel(PermuteArgs a, uint32_
             sm + i * row_bytes),
         "l"(x + (t0 + i) * (int64_t)row_bytes), "r"(row_bytes), "r"(b)
         : "memory");
+  pdl_wait();   // row_of comes from map_scatter
   // bounded wait for the rows to land
   uint32_t done = 0;
   const uint64_t start = now_ns();
@@ -415,17 +428,30 @@ cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   const int nblk = (int)((a.T + kMapBlock - 1) / kMapBlock);
   const size_t bm_bytes = (size_t)a.E * 8 * sizeof(uint32_t);
   map_count_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a);
-  map_scatter_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a, nblk);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nblk);
+  cfg.blockDim = dim3(kMapBlock);
+  cfg.dynamicSmemBytes = bm_bytes;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, map_scatter_kernel, a, nblk);
+  if (e != cudaSuccess) return e;
   const uint32_t row_bytes = (uint32_t)a.d * (a.dtype == MOE_BF16 ? 2u : 4u);
   int tpc = kPermTokens;
   while (tpc > 1 && (uint32_t)tpc * row_bytes > kPermSmemCap) --tpc;
   const size_t smem = (size_t)tpc * row_bytes;
   if (smem > 200 * 1024) return cudaErrorInvalidValue;  // rows wider than the bulk path holds
-  cudaError_t e = cudaFuncSetAttribute(permute_bulk_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(permute_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
   if (e != cudaSuccess) return e;
-  permute_bulk_kernel<<<(unsigned)((a.T + tpc - 1) / tpc), 32, smem, s>>>(a, row_bytes, tpc);
-  return cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)((a.T + tpc - 1) / tpc));
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = smem;
+  return cudaLaunchKernelEx(&cfg, permute_bulk_kernel, a, row_bytes, tpc);
 }
 
 cudaError_t launch_unpermute(const UnpermuteArgs &a, cudaStream_t s) {
