@@ -170,6 +170,17 @@ def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = Non
 
 # ---------------------------------------------------------------------------
 
+def code_text(path: str) -> str:
+    """A source file without its // comments and blank lines: the key under
+    which profiles/traffic.json records the counters of that code."""
+    out = []
+    for line in open(path):
+        line = line.split("//", 1)[0].strip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def launches_per_step(cfg, etp: int = 1) -> int:
     n = (2 if cfg.dtype == "bf16" else 1)  # router: logits GEMM + Top-K (fp32: one fused kernel)
     n += 1 if cfg.drop else 0             # capacity
@@ -345,7 +356,7 @@ def main():
         import hashlib
         ent = json.load(open(tr_path)).get(f"{cfg.name}:grouped_gemm")
         src = os.path.join(ROOT, "token_dispatch_expert_moe_gb300", "csrc", "gemm_tc.cu")
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = hashlib.sha256(code_text(src).encode()).hexdigest()[:16]
         if ent is not None and ent.get("source_sha") == sha:   # counters of this very kernel
             traffic = ent["bytes"]
 

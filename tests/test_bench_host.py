@@ -56,3 +56,25 @@ def test_launch_counts():
     assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 10
     assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 15
     assert bench.launches_per_step(get_config("tiny_f32")) == 7
+
+
+def test_traffic_key_ignores_comments_only(tmp_path):
+    import bench
+    a, b, c = tmp_path / "a.cu", tmp_path / "b.cu", tmp_path / "c.cu"
+    a.write_text("int f() {\n  return 1;  // one\n}\n")
+    b.write_text("// header\nint f() {\n\n  return 1;\n}\n")
+    c.write_text("int f() {\n  return 2;\n}\n")
+    assert bench.code_text(str(a)) == bench.code_text(str(b))
+    assert bench.code_text(str(a)) != bench.code_text(str(c))
+
+
+def test_traffic_record_matches_current_gemm_source():
+    """profiles/traffic.json must describe the grouped GEMM as it is now;
+    after a code change its counters are stale and have to be taken again."""
+    import hashlib
+    import json
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    rec = json.load(open(os.path.join(root, "profiles", "traffic.json")))["mixtral_8x22b:grouped_gemm"]
+    src = os.path.join(root, "token_dispatch_expert_moe_gb300", "csrc", "gemm_tc.cu")
+    assert rec["source_sha"] == hashlib.sha256(bench.code_text(src).encode()).hexdigest()[:16]

@@ -6,18 +6,25 @@
 // rows of group g are [offsets[g], offsets[g+1]) of the permuted buffers;
 // offsets stay on the device and every CTA derives the tile list from them.
 //
-// One persistent, warp-specialised kernel template, one CTA per SM:
-//   warp 0      TMA producer: 128B-swizzled boxes into a 4-stage smem ring;
+// Two persistent, warp-specialised kernel templates (192 threads, one CTA per
+// SM):
+//   warp 0      TMA producer: 128B-swizzled boxes into a shared-memory ring;
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
-//               fp32 accumulate), M = 128, N = 128..256, K = 16 per
-//               instruction, 4 per 64-deep stage; tcgen05.commit frees the
-//               stage and, at the end of a tile, hands the accumulator over;
+//               fp32 accumulate), K = 16 per instruction, 4 per 64-deep
+//               stage; tcgen05.commit frees the stage and, at the end of a
+//               tile, hands the accumulator over;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
-//               quarter per warp), fused math, stores to global memory.
-// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile overlap
-// the mainloop of the next.
+//               quarter per warp), fused math, 32-row slabs staged in swizzled
+//               shared memory and written with TMA bulk stores.
+// tc_gemm_kernel: one CTA per tile, M = 128, 4 stages of 48 KB (used by the
+// router GEMM and when CTA pairs are disabled). tc_gemm_pair_kernel: clusters
+// of two CTAs on one TPC issue tcgen05.mma.cta_group::2 (M = 256, each CTA
+// holding its 128 rows of A and half of B), 6 stages of 32 KB per CTA; the
+// even CTA's barriers see both CTAs' TMA bytes and its MMA warp issues for the
+// pair. Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
+// overlap the mainloop of the next.
 //
-// The six GEMMs (A: M x K, B: N x K, per group g):
+// The GEMMs (A: M x K, B: N x K, per group g):
 //   GU      [G|U] = Xp W_gu[g]^T, SwiGLU epilogue H = silu(G) U (+ A_save)
 //   DOWN    Yp    = H W_down[g]^T
 //   DH      dH    = dYp W_down[g]  -> epilogue dA = [dG | dU]   (B MN-major)
@@ -29,8 +36,10 @@
 //           vector rides along as a second B box); fp32 logits out.
 // In GU/DOWN/DH/DX a tile's rows past the group's end belong to the next
 // group (or are zero-filled past the buffer); only their outputs are masked.
-// In WGD/WGU the reduction runs over the group's rows, so K rows past the end
-// are zeroed in shared memory before the MMA reads them.
+// In WGD/WGU the reduction runs over the group's rows: the loads go through
+// per-group tensor maps whose outer extent is the group's row count (written
+// on the device by group_maps_kernel), so the TMA zero-fills K rows past the
+// group's end.
 //
 // Every wait on an mbarrier is bounded (about two seconds of
 // %globaltimer); on expiry the kernel records MOE_ERR_TIMEOUT in the status
