@@ -99,3 +99,23 @@ def test_invalid_arguments_rejected_on_host(L):
         L.moe_expert_ffn_bwd(1, 32, 128, 128, 4, fake, fake, fake, fake, fake, fake, fake, fake,
                              fake, fake, fake, fake, 0, ws_bytes=L.MOE_FFN_BWD_WORKSPACE_BYTES - 256)
     assert e.value.code == 1
+
+
+def test_plain_c_caller(L, tmp_path):
+    """The header is plain C: a C program compiled against include/moe.h
+    alone links libmoe.so and runs its host-side checks (no device access)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from token_dispatch_expert_moe_gb300 import build
+    exe = str(tmp_path / "c_abi_probe")
+    libdir = os.path.dirname(build.LIB)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_probe.c"), "-o", exe,
+                        build.LIB, "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "c abi probe ok" in r.stdout
