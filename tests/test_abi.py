@@ -119,3 +119,13 @@ def test_plain_c_caller(L, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "c abi probe ok" in r.stdout
+
+
+def test_binding_constants_match_header(L):
+    txt = open(os.path.join(ROOT, "include", "moe.h")).read()
+    m = re.search(r"#define\s+MOE_FFN_BWD_WORKSPACE_BYTES\s+(\d+)u?", txt)
+    assert m and int(m.group(1)) == L.MOE_FFN_BWD_WORKSPACE_BYTES
+    m = re.search(r"#define\s+MOE_PERMUTE_NOALLOC_MAX_TOKENS\s+(\d+)", txt)
+    assert m and int(m.group(1)) == 131072
+    assert re.search(r"MOE_F32\s*=\s*0", txt) and re.search(r"MOE_BF16\s*=\s*1", txt)
+    assert (L.MOE_F32, L.MOE_BF16) == (0, 1)
