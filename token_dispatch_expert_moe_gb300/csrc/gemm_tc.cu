@@ -843,10 +843,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 //   MMA (even CTA only): commits multicast to both CTAs' empty / tfull;
 //   epilogue (both CTAs): own TMEM rows, then arrive on the even CTA's tempty
 //     (8 arrivals: 4 warps x 2 CTAs).
-constexpr int kPairStages = 6;
-constexpr int kPairStageBytes = 32768;
+// NSUB = 2: a pair tile covers two adjacent N tiles that share the A
+// operand (one A box and two B boxes per stage, 48 KB, 4 stages), one TMEM
+// accumulator each. Less shared memory per unit of MMA work, so the same
+// ring bytes cover a longer load latency; the two accumulators are the two
+// TMEM buffers, so the epilogue no longer overlaps the next tile's mainloop
+// (used where the epilogue is short).
+template <int NSUB> constexpr int pair_stages() { return NSUB == 1 ? 6 : 4; }
+template <int NSUB> constexpr int pair_stage_bytes() { return kABytes + NSUB * 16384; }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int NSUB = 1>
 __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const SharedState &st, int pt,
                                                  int rank) {
   Tile t;
@@ -861,19 +867,24 @@ __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const Shared
   } else {
     t = decode_tile<MODE, BN>(p, st, pt);
     t.m = 2 * t.m + rank;
+    t.n *= NSUB;   // first of the tile's NSUB N tiles
   }
   return t;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
   using TR = ModeTraits<MODE>;
+  static_assert(NSUB == 1 || !TR::red, "weight-gradient tiles are single");
+  constexpr int kPairStages = pair_stages<NSUB>();
+  constexpr int kPairStageBytes = pair_stage_bytes<NSUB>();
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
   constexpr int HALF_N = MMA_N / 2;
+  static_assert(NSUB == 1 || HALF_N * BK * 2 == 16384, "two B halves of 16 KB per stage");
   constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
   constexpr int B_HALF_BOXES = TR::b_mn ? HALF_N / 64 : 1;
-  constexpr uint32_t kOwnTx = kABytes + HALF_N * BK * 2;   // one CTA's bytes per stage
+  constexpr uint32_t kOwnTx = kABytes + NSUB * HALF_N * BK * 2;   // one CTA's bytes per stage
   constexpr uint32_t kTx = 2u * kOwnTx;
   constexpr uint32_t kIdesc = instr_desc(256, MMA_N, TR::a_mn, TR::b_mn);
 
@@ -896,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         if (p.offsets[g + 1] < p.offsets[g]) bad = true;
       total = p.n_groups * (p.M_fixed / 256) * (p.N / BN);   // 256-row pair tiles
     } else {
-      const int NT = p.N / (MODE == GU ? 128 : BN);
+      const int NT = p.N / (MODE == GU ? 128 : BN) / NSUB;
       for (int g = 0; g < p.n_groups; ++g) {
         const int rows = p.offsets[g + 1] - p.offsets[g];
         if (rows < 0) bad = true;
@@ -948,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 #pragma unroll
       for (int i = 0; i < kPairStages; ++i) last_phase[i] = -1;
       for (int pt = cid; pt < total && !st.abort; pt += ncl) {
-        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
+        const Tile t = decode_pair_tile<MODE, BN, NSUB>(p, st, pt, (int)rank);
         const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kPairStages;
@@ -977,15 +988,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           } else {
             tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
-            if constexpr (MODE == GU) {   // even CTA: gate rows, odd CTA: up rows
-              tma_load_2d_pair(sb, &p.tmB, bar, kb * BK, (int)(gb + (int64_t)rank * p.F + t.n * 128));
-            } else if constexpr (TR::b_mn) {
 #pragma unroll
-              for (int b = 0; b < B_HALF_BOXES; ++b)
-                tma_load_2d_pair(sb + b * 8192, &p.tmB, bar,
-                                 t.n * BN + (int)rank * HALF_N + 64 * b, (int)(gb + kb * BK));
-            } else {
-              tma_load_2d_pair(sb, &p.tmB, bar, kb * BK, (int)(gb + t.n * BN + (int)rank * HALF_N));
+            for (int j = 0; j < NSUB; ++j) {   // B half of each of the tile's N tiles
+              const uint32_t sbj = sb + j * 16384;
+              const int n = t.n + j;
+              if constexpr (MODE == GU) {   // even CTA: gate rows, odd CTA: up rows
+                tma_load_2d_pair(sbj, &p.tmB, bar, kb * BK, (int)(gb + (int64_t)rank * p.F + n * 128));
+              } else if constexpr (TR::b_mn) {
+#pragma unroll
+                for (int b = 0; b < B_HALF_BOXES; ++b)
+                  tma_load_2d_pair(sbj + b * 8192, &p.tmB, bar,
+                                   n * BN + (int)rank * HALF_N + 64 * b, (int)(gb + kb * BK));
+              } else {
+                tma_load_2d_pair(sbj, &p.tmB, bar, kb * BK, (int)(gb + n * BN + (int)rank * HALF_N));
+              }
             }
           }
         }
@@ -1007,11 +1023,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       int it = 0, tcount = 0;
       bool issued_any = false;
       for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
-        const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, 0);
+        const Tile t = decode_pair_tile<MODE, BN, NSUB>(p, st, pt, 0);
         const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
-        const int buf = tcount & 1;
-        const uint32_t use = (tcount >> 1) & 1;
-        if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2))) break;
+        // NSUB = 1: the two TMEM buffers alternate between tiles; NSUB = 2:
+        // every tile uses both (buffer j for its j-th N tile)
+        const int buf = NSUB == 1 ? (tcount & 1) : 0;
+        const uint32_t use = NSUB == 1 ? ((tcount >> 1) & 1) : (tcount & 1);
+        bool waited = true;
+#pragma unroll
+        for (int j = 0; j < NSUB; ++j)
+          waited = waited && __all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf + j]),
+                                                                  use ^ 1, p.status, 2));
+        if (!waited) break;
         tc_fence_after();
         const uint32_t dcol = tmem + buf * 256;
         bool ok = true;
@@ -1031,9 +1054,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
               uint64_t ad, bd;
               if constexpr (TR::a_mn) ad = smem_desc(sa + ks * 2048, 8192, 1024);
               else ad = smem_desc(sa + ks * 32, 16, 1024);
-              if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
-              else bd = smem_desc(sb + ks * 32, 16, 1024);
-              tc_mma_pair(dcol, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+              for (int j = 0; j < NSUB; ++j) {
+                const uint32_t sbj = sb + j * 16384;
+                if constexpr (TR::b_mn) bd = smem_desc(sbj + ks * 2048, 8192, 1024);
+                else bd = smem_desc(sbj + ks * 32, 16, 1024);
+                tc_mma_pair(dcol + j * 256, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+              }
             }
             tc_commit_pair_both(smem_u32(&st.empty[s]));
             issued_any = true;
@@ -1041,7 +1068,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) tc_commit_pair_both(smem_u32(&st.tfull[buf]));
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < NSUB; ++j) tc_commit_pair_both(smem_u32(&st.tfull[buf + j]));
+        }
         __syncwarp();
       }
       if (lane == 0 && issued_any) {
@@ -1059,17 +1089,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     Stager sg{staging + (warp - 2) * 2 * kStageOutBytes, 0};
     uint32_t ephase = 0;
     int tcount = 0;
-    for (int pt = cid; pt < total && !st.abort; pt += ncl, ++tcount) {
-      const Tile t = decode_pair_tile<MODE, BN>(p, st, pt, (int)rank);
-      const int buf = tcount & 1;
-      const uint32_t use = (tcount >> 1) & 1;
-      if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
-      epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&st.tempty[buf]), 0));
+    bool stop = false;
+    for (int pt = cid; pt < total && !st.abort && !stop; pt += ncl, ++tcount) {
+      const Tile t0 = decode_pair_tile<MODE, BN, NSUB>(p, st, pt, (int)rank);
+#pragma unroll 1
+      for (int j = 0; j < NSUB; ++j) {   // the tile's N tiles, one TMEM buffer each
+        const int buf = NSUB == 1 ? (tcount & 1) : j;
+        const uint32_t use = NSUB == 1 ? ((tcount >> 1) & 1) : (tcount & 1);
+        if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        Tile t = t0;
+        t.n = t0.n + j;
+        const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
+        epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&st.tempty[buf]), 0));
+      }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncwarp();
@@ -1199,13 +1238,12 @@ cudaError_t launch_mode(TcParams p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-constexpr size_t kPairSmemBytes =
-    kPairStages * kPairStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
-
-template <int MODE, int BN>
+template <int MODE, int BN, int NSUB = 1>
 cudaError_t launch_pair(TcParams p, cudaStream_t s) {
   p.fault_stall = fault_stall();
-  auto k = tc_gemm_pair_kernel<MODE, BN>;
+  auto k = tc_gemm_pair_kernel<MODE, BN, NSUB>;
+  constexpr size_t kPairSmemBytes = (size_t)pair_stages<NSUB>() * pair_stage_bytes<NSUB>() +
+                                    kEpiStagingBytes + sizeof(SharedState) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1239,8 +1277,14 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
   const bool bn256 = !(MODE == GU || p.N % 256 != 0);
   if constexpr (MODE != RT) {
     const bool red = (MODE == WGD || MODE == WGU);
-    if (pair_enabled() && (!red || p.M_fixed % 256 == 0))
+    if (pair_enabled() && (!red || p.M_fixed % 256 == 0)) {
+      // two N tiles per pair tile where the epilogue (no longer overlapped
+      // with the next tile's mainloop) is short against a long K loop: the
+      // down projection and dXp with K >= 8192 (128 K blocks)
+      if constexpr (MODE == DOWN || MODE == DX)
+        if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192) return launch_pair<MODE, 256, 2>(p, s);
       return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
+    }
   }
   return bn256 ? launch_mode<MODE, 256>(p, s) : launch_mode<MODE, 128>(p, s);
 }
