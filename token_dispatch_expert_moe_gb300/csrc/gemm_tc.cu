@@ -236,6 +236,32 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Two 32-column TMEM loads (at ta and tb) in flight before one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(r[i]);
+    b[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family format):
 // start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
 // byte offset >> 4 in 32-45, descriptor version 1 at bit 46, layout
@@ -420,34 +446,32 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
     // the group's end takes the row-store path below)
     const int y = t.row0 + t.m * BM + q * 32;
     if constexpr (MODE == GU) {
+      const bool save = p.out1 != nullptr;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {  // 64 gate/up columns per chunk
-        uint32_t w[32];
+        uint32_t wh[32], wg[32], wu[32];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          float g[32], u[32];
-          tmem_ld32(tbase + c * 64 + hh * 32, g);
-          tmem_ld32(tbase + 128 + c * 64 + hh * 32, u);
+          float g[32], u[32], h[32];
+          tmem_ld32x2(tbase + c * 64 + hh * 32, tbase + 128 + c * 64 + hh * 32, g, u);
+          if (save) {
+            pack_bf16(g, wg, hh * 16);
+            pack_bf16(u, wu, hh * 16);
+          }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) g[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
-          pack_bf16(g, w, hh * 16);
+          for (int i = 0; i < 32; ++i) h[i] = g[i] * __frcp_rn(1.0f + __expf(-g[i])) * u[i];
+          pack_bf16(h, wh, hh * 16);
         }
         uint8_t *b = stage_begin(sg, lane);
-        stage_row(b, lane, w);
+        stage_row(b, lane, wh);
         stage_store(b, &p.tmO0, t.n * 128 + c * 64, y, lane);
-        if (p.out1 != nullptr) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {  // G, then U
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              float v[32];
-              tmem_ld32(tbase + half * 128 + c * 64 + hh * 32, v);
-              pack_bf16(v, w, hh * 16);
-            }
-            uint8_t *b2 = stage_begin(sg, lane);
-            stage_row(b2, lane, w);
-            stage_store(b2, &p.tmO1, half * p.F + t.n * 128 + c * 64, y, lane);
-          }
+        if (save) {   // A_save = [G | U]
+          uint8_t *b2 = stage_begin(sg, lane);
+          stage_row(b2, lane, wg);
+          stage_store(b2, &p.tmO1, t.n * 128 + c * 64, y, lane);
+          uint8_t *b3 = stage_begin(sg, lane);
+          stage_row(b3, lane, wu);
+          stage_store(b3, &p.tmO1, p.F + t.n * 128 + c * 64, y, lane);
         }
       }
     } else if constexpr (MODE == DOWN) {
