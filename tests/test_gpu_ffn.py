@@ -141,3 +141,23 @@ def test_single_cta_and_pair_kernels_agree(pair):
     r = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True,
                        text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+
+
+@pytest.mark.parametrize("rows,d,F", [
+    ([8300, 8100], 512, 512),   # weight gradients: >= 8192 rows per group (two N tiles per pair tile)
+    ([300, 0, 200], 8192, 512),  # dH with K = d = 8192 (two N tiles per pair tile)
+    ([300, 200], 512, 4096),     # dXp with K = 2F = 8192 (two N tiles per pair tile)
+])
+def test_ffn_backward_long_k(rows, d, F):
+    """The long-K shapes that switch the CTA-pair GEMMs to two N tiles per
+    pair tile, against the oracle."""
+    L = lib()
+    G = len(rows)
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    n = int(offsets[-1])
+    Xp = normal_bf16(7, 101, (n, d))
+    W_gu = normal_bf16(7, 102, (G, 2 * F, d), 1 / np.sqrt(d))
+    W_down = normal_bf16(7, 103, (G, d, F), 1 / np.sqrt(F))
+    rnd = O.act_rounder("bf16", True)
+    dYp = rnd(O.decode(normal_bf16(7, 104, (n, d))) * 0.5)
+    _check_bwd(L, "bf16", Xp, offsets, W_gu, W_down, dYp, d, F)

@@ -881,10 +881,10 @@ __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const Shared
                                                  int rank) {
   Tile t;
   if constexpr (ModeTraits<MODE>::red) {
-    const int MT2 = p.M_fixed / 256, NT = p.N / BN;
+    const int MT2 = p.M_fixed / 256, NT = p.N / BN / NSUB;
     t.g = pt / (MT2 * NT);
     const int loc = pt % (MT2 * NT);
-    t.n = loc / MT2;
+    t.n = (loc / MT2) * NSUB;
     t.m = 2 * (loc % MT2) + rank;
     t.row0 = p.offsets[t.g];
     t.rows = p.offsets[t.g + 1] - t.row0;
@@ -900,7 +900,6 @@ template <int MODE, int BN, int NSUB>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
   using TR = ModeTraits<MODE>;
-  static_assert(NSUB == 1 || !TR::red, "weight-gradient tiles are single");
   constexpr int kPairStages = pair_stages<NSUB>();
   constexpr int kPairStageBytes = pair_stage_bytes<NSUB>();
   constexpr int MMA_N = (MODE == GU) ? 256 : BN;
@@ -929,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     if constexpr (TR::red) {
       for (int g = 0; g < p.n_groups; ++g)
         if (p.offsets[g + 1] < p.offsets[g]) bad = true;
-      total = p.n_groups * (p.M_fixed / 256) * (p.N / BN);   // 256-row pair tiles
+      total = p.n_groups * (p.M_fixed / 256) * (p.N / BN / NSUB);   // 256-row pair tiles
     } else {
       const int NT = p.N / (MODE == GU ? 128 : BN) / NSUB;
       for (int g = 0; g < p.n_groups; ++g) {
@@ -1007,8 +1006,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
             for (int b = 0; b < A_BOXES; ++b)
               tma_load_2d_pair(sa + b * 8192, mA, bar, t.m * BM + 64 * b, kb * BK);
 #pragma unroll
-            for (int b = 0; b < B_HALF_BOXES; ++b)
-              tma_load_2d_pair(sb + b * 8192, mB, bar, t.n * BN + (int)rank * HALF_N + 64 * b, kb * BK);
+            for (int j = 0; j < NSUB; ++j)
+#pragma unroll
+              for (int b = 0; b < B_HALF_BOXES; ++b)
+                tma_load_2d_pair(sb + j * 16384 + b * 8192, mB, bar,
+                                 (t.n + j) * BN + (int)rank * HALF_N + 64 * b, kb * BK);
           } else {
             tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
@@ -1305,8 +1307,11 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
       // two N tiles per pair tile where the epilogue (no longer overlapped
       // with the next tile's mainloop) is short against a long K loop: the
       // down projection and dXp with K >= 8192 (128 K blocks)
-      if constexpr (MODE == DOWN || MODE == DX)
+      if constexpr (MODE == DOWN || MODE == DX || MODE == DH)
         if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192) return launch_pair<MODE, 256, 2>(p, s);
+      if constexpr (red)   // K = a group's rows: the same test on the mean rows per group
+        if (bn256 && (p.N / 256) % 2 == 0 && p.max_rows / p.n_groups >= 8192)
+          return launch_pair<MODE, 256, 2>(p, s);
       return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
     }
   }
