@@ -5,7 +5,12 @@
 // capacity factor), "key modules" and the quoted section 3.3 (drops are
 // decided inside each sub-sequence; sub-sequence dropping is the default).
 //
-// The softmax and Top-K arithmetic is specified in softmax.cuh.
+// bf16 layers compute the logits (and the shared-expert gate logit) on the
+// tensor cores (router mode of the grouped GEMM, gemm_tc.cu) and then run
+// topk_from_logits_kernel; fp32 layers use router_fused_kernel, which does
+// the logits GEMV, softmax and Top-K in one pass. capacity_kernel applies the
+// drop rule per (sub-sequence, expert). The softmax and Top-K arithmetic is
+// specified in softmax.cuh.
 #include "common.cuh"
 #include "softmax.cuh"
 
