@@ -76,23 +76,33 @@ def test_permute_padded_edge_cases(case):
     _check_padded(L, cfg, x, idx, keep)
 
 
-@pytest.mark.parametrize("name", ["mixtral_8x22b@small", "mixtral_8x22b_g8t8@small"])
-def test_layer_padded_matches_oracle(name):
+@pytest.mark.parametrize("name,etp", [("mixtral_8x22b@small", 1), ("mixtral_8x22b_g8t8@small", 1),
+                                      ("mixtral_8x22b_g8t8@small", 2)])
+def test_layer_padded_matches_oracle(name, etp):
     L = lib()
     from token_dispatch_expert_moe_gb300.layer import MoELayer
     cfg = dataclasses.replace(get_config(name), backward=True)
     inp = make_inputs(cfg, need_backward=True)
     w = {k: dev(v) for k, v in inp.items() if k not in ("x", "dout")}
-    layer = MoELayer(cfg, w, backward=True, layout="padded")
+    layer = MoELayer(cfg, w, backward=True, layout="padded", etp=etp)
     x, dout = dev(inp["x"]), dev(inp["dout"])
     for _ in range(2):   # the second step runs on padding rows the first step left behind
         out = layer.forward(x)
         g = layer.backward(dout)
     rc, info = L.moe_get_status(layer.ws)
     assert rc == 0, (rc, hex(info))
-    f = O.layer_forward(cfg, inp)
+    f = O.layer_forward(cfg, inp, etp=etp)
     assert np.array_equal(host(layer.counts), f["counts"])
     assert_close("out", host(out), f["out"], cfg.dtype)
-    gr = O.layer_backward(cfg, inp, f)
-    for k in ("dx", "dW_r", "dW_gu", "dW_down"):
+    gr = O.layer_backward(cfg, inp, f, etp=etp)
+    for k in ("dx", "dW_r"):
         assert_close(k, host(g[k]), gr[k], cfg.dtype)
+    if etp == 1:
+        dW_gu, dW_down = g["dW_gu"], g["dW_down"]
+    else:   # per-shard weight gradients back to the full layouts
+        Fl = g["dW_gu"][0].shape[1] // 2
+        dW_gu = torch.cat([torch.cat([s_[:, :Fl] for s_ in g["dW_gu"]], 1),
+                           torch.cat([s_[:, Fl:] for s_ in g["dW_gu"]], 1)], 1)
+        dW_down = torch.cat(g["dW_down"], 2)
+    assert_close("dW_gu", host(dW_gu), gr["dW_gu"], cfg.dtype)
+    assert_close("dW_down", host(dW_down), gr["dW_down"], cfg.dtype)
