@@ -51,21 +51,26 @@ __global__ void __launch_bounds__(256) dl_kernel(RouteBwdArgs a) {
 }
 
 // dx_router[t, j] = dx_in[t, j] + sum_c dl[t, c] W[c, j]  (row c = E is w_sg
-// with dl = dz). A CTA takes 128 tokens and 256 columns: the dl tile stays in
-// shared memory in its natural [token][c] layout while four 64-column tiles
-// of W (converted to fp32) pass through. Each thread computes 8 tokens x 4
-// columns: per 4 values of c it reads 8 float4 of dl (broadcast within each
-// half-warp) and 4 float4 of W for 128 FMAs. The sum over c runs in
-// ascending order per output.
-constexpr int kDxT = 128, kDxJ = 64, kDxSub = 4;
-template <int CP> constexpr size_t dx_smem_bytes() { return (size_t)(kDxT + kDxJ) * CP * sizeof(float); }
+// with dl = dz). A CTA takes 128 tokens and `nsub` consecutive 64-column
+// tiles of W: the dl tile stays in shared memory in its natural [token][c]
+// layout, and the W tiles (converted to fp32) pass through a double buffer,
+// the next one loaded into registers while the current one is used. Each
+// thread computes 8 tokens x 4 columns: per 4 values of c it reads 8 float4
+// of dl (broadcast within each half-warp) and 4 float4 of W for 128 FMAs.
+// The sum over c runs in ascending order per output.
+constexpr int kDxT = 128, kDxJ = 64;
+template <int CP> constexpr size_t dx_smem_bytes() {
+  return (size_t)(kDxT + 2 * kDxJ) * CP * sizeof(float);
+}
 
 template <typename T, int CP>
-__global__ void __launch_bounds__(256) dx_kernel(RouteBwdArgs a) {
+__global__ void __launch_bounds__(256, 2) dx_kernel(RouteBwdArgs a, int nsub) {
   extern __shared__ __align__(16) float dx_smem[];
-  float *dls = dx_smem;               // [kDxT][CP]
-  float *Ws = dx_smem + kDxT * CP;    // [CP][kDxJ]
+  float *dls = dx_smem;                       // [kDxT][CP]
+  float *Wbuf = dx_smem + kDxT * CP;          // [2][CP][kDxJ]
   constexpr int NV = Vec<T>::N;
+  constexpr int VPR = kDxJ / NV;              // 16-byte vectors per W row of a tile
+  constexpr int WV = (CP * VPR + 255) / 256;  // W vectors per thread per tile
   const int E = a.E;
   const int C = E + (a.w_sg != nullptr ? 1 : 0);
   const int64_t t0 = (int64_t)blockIdx.x * kDxT;
@@ -78,27 +83,57 @@ __global__ void __launch_bounds__(256) dx_kernel(RouteBwdArgs a) {
     if (t < a.T && c < C) v = c < E ? a.dl[t * E + c] : a.dz[t];
     dls[i] = v;
   }
+  uint4 wr[WV];
+  auto fetch_w = [&](int j0) {   // this thread's vectors of the W tile at column j0
+#pragma unroll
+    for (int q = 0; q < WV; ++q) {
+      const int i = threadIdx.x + q * 256;
+      const int c = i / VPR, j = j0 + (i - c * VPR) * NV;
+      wr[q] = (i < CP * VPR && c < C && j < a.d)   // d is a multiple of NV
+                  ? *reinterpret_cast<const uint4 *>((c < E ? W + (int64_t)c * a.d : wsg) + j)
+                  : make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto stash_w = [&](float *Ws) {
+#pragma unroll
+    for (int q = 0; q < WV; ++q) {
+      const int i = threadIdx.x + q * 256;
+      if (i < CP * VPR) {
+        const int c = i / VPR, jv = (i - c * VPR) * NV;
+        float v[NV];
+        unpack16<T>(wr[q], v);
+#pragma unroll
+        for (int k = 0; k < NV; k += 4)
+          *reinterpret_cast<float4 *>(&Ws[c * kDxJ + jv + k]) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+      }
+    }
+  };
+  const int jfirst = blockIdx.y * nsub * kDxJ;
+  if (jfirst >= a.d) return;
+  fetch_w(jfirst);
+  stash_w(Wbuf);
+  __syncthreads();   // dl tile and the first W tile
   const int tq = threadIdx.x >> 4;   // token octet 0..15
   const int jq = threadIdx.x & 15;   // column quad 0..15
-  for (int sub = 0; sub < kDxSub; ++sub) {
-    const int j0 = (blockIdx.y * kDxSub + sub) * kDxJ;
+  for (int sub = 0; sub < nsub; ++sub) {
+    const int j0 = jfirst + sub * kDxJ;
     if (j0 >= a.d) break;   // the same for every thread of the CTA
-    __syncthreads();        // dl tile written; the previous W tile consumed
-    for (int i = threadIdx.x; i < CP * (kDxJ / NV); i += blockDim.x) {
-      const int c = i / (kDxJ / NV), jv = (i - c * (kDxJ / NV)) * NV;
-      const int j = j0 + jv;
-      float v[NV];
-      if (c < C && j < a.d) {   // d is a multiple of NV: a vector is all in or all out
-        load16<T>((c < E ? W + (int64_t)c * a.d : wsg) + j, v);
-      } else {
+    const bool next = sub + 1 < nsub && j0 + kDxJ < a.d;
+    if (next) fetch_w(j0 + kDxJ);   // in flight while this tile is used
+    const float *Ws = Wbuf + (sub & 1) * CP * kDxJ;
+    const int j = j0 + jq * 4;
+    float4 xin[8];
+    if (a.dx_in != nullptr && j < a.d) {
 #pragma unroll
-        for (int q = 0; q < NV; ++q) v[q] = 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        const int64_t t = t0 + tq * 8 + i;
+        xin[i] = t < a.T ? *reinterpret_cast<const float4 *>(a.dx_in + t * a.d + j)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    } else {
 #pragma unroll
-      for (int q = 0; q < NV; q += 4)
-        *reinterpret_cast<float4 *>(&Ws[c * kDxJ + jv + q]) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      for (int i = 0; i < 8; ++i) xin[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
     float acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -122,20 +157,20 @@ __global__ void __launch_bounds__(256) dx_kernel(RouteBwdArgs a) {
           for (int n = 0; n < 4; ++n) acc[i][n] = fmaf(d4[k], w[k][n], acc[i][n]);
       }
     }
-    const int j = j0 + jq * 4;
     if (j < a.d) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int64_t t = t0 + tq * 8 + i;
         if (t >= a.T) break;
         float4 o = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        if (a.dx_in != nullptr) {
-          const float4 xi = *reinterpret_cast<const float4 *>(a.dx_in + t * a.d + j);
-          o.x += xi.x; o.y += xi.y; o.z += xi.z; o.w += xi.w;
+        if (a.dx_in != nullptr) {   // (0 + sum) + dx_in, as before
+          o.x += xin[i].x; o.y += xin[i].y; o.z += xin[i].z; o.w += xin[i].w;
         }
         *reinterpret_cast<float4 *>(a.dx_router + t * a.d + j) = o;
       }
     }
+    if (next) stash_w(Wbuf + ((sub + 1) & 1) * CP * kDxJ);
+    __syncthreads();   // the next tile is in place; this one's reads are done
   }
 }
 
@@ -275,12 +310,19 @@ size_t route_bwd_workspace_bytes(int64_t T, int d, int E) {
 
 template <typename T, int CP>
 void launch_cp_t(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk) {
-  constexpr int kSubCols = kDxJ * kDxSub;
-  dim3 gdx((unsigned)((a.T + kDxT - 1) / kDxT), (unsigned)((a.d + kSubCols - 1) / kSubCols));
+  // enough CTAs for two per SM; each takes nsub of the ceil(d / 64) column tiles
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ttiles = (int)((a.T + kDxT - 1) / kDxT), jtiles = (a.d + kDxJ - 1) / kDxJ;
+  int ysplit = (2 * (sms > 0 ? sms : 148) + ttiles - 1) / ttiles;
+  ysplit = ysplit < 1 ? 1 : (ysplit > jtiles ? jtiles : ysplit);
+  const int nsub = (jtiles + ysplit - 1) / ysplit;
+  dim3 gdx((unsigned)ttiles, (unsigned)((jtiles + nsub - 1) / nsub));
   dim3 gw((unsigned)nchunk, (unsigned)((a.d + kCols - 1) / kCols));
   auto k = dx_kernel<T, CP>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dx_smem_bytes<CP>());
-  k<<<gdx, 256, dx_smem_bytes<CP>(), s>>>(a);
+  k<<<gdx, 256, dx_smem_bytes<CP>(), s>>>(a, nsub);
   wgrad_partial_kernel<T, CP><<<gw, 256, 0, s>>>(a, chunk);
 }
 
