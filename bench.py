@@ -182,17 +182,25 @@ def code_text(path: str) -> str:
 
 
 def launches_per_step(cfg, etp: int = 1) -> int:
-    n = (2 if cfg.dtype == "bf16" else 1)  # router: logits GEMM + Top-K (fp32: one fused kernel)
+    bf16 = cfg.dtype == "bf16"
+    n = 2 if bf16 else 1                   # router: logits GEMM + Top-K (fp32: one fused kernel)
     n += 1 if cfg.drop else 0             # capacity
     n += 3                                 # map count, map scatter, row copy
     n += 2 * etp + (1 if etp > 1 else 0)   # routed grouped GEMMs per F-shard [+ partial sum]
     n += 2 if cfg.Fs else 0                # shared expert
     n += 1                                 # un-permute
     if cfg.backward:
+        gm = 2 if bf16 else 0              # group tensor maps of the two weight-gradient GEMMs
         n += 1                             # un-permute backward
-        n += 4 * etp + (1 if etp > 1 else 0)   # dH, dX, dW_down, dW_gu per shard [+ dXp sum]
-        n += 4 if cfg.Fs else 0
-        n += 4 + (1 if cfg.bias else 0)    # router backward
+        n += (4 + gm) * etp + (1 if etp > 1 else 0)   # dH, dX, dW_down, dW_gu per shard [+ dXp sum]
+        n += (4 + gm) if cfg.Fs else 0
+        if bf16 and cfg.d % 256 == 0:      # router backward on the tensor cores:
+            # dl, dl planes, [W_r planes + dx GEMM | dx kernel with the shared-expert addend],
+            # group maps, dW_r GEMM, plane sum
+            n += 6 + (0 if cfg.Fs else 1)
+        else:
+            n += 4                         # dl, dx, dW_r partials, reduce
+        n += 1 if cfg.bias else 0          # db_r
         n += 1                             # permute backward
     return n
 

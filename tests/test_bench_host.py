@@ -53,8 +53,12 @@ def test_launch_counts():
     import bench
     from synthetic import get_config
     assert bench.launches_per_step(get_config("mixtral_8x22b")) == 9
-    assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 10
-    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 15
+    # llama: fwd 8; bwd: un-permute 1, FFN 4 + 2 maps, router 7, permute 1
+    assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 15
+    # qwen: fwd 10; bwd: 1 + (6 + 6) + router 6 + db 1 + permute 1
+    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 21
+    # g8t8: fwd 9; bwd 1 + 6 + 7 + 1
+    assert bench.launches_per_step(get_config("mixtral_8x22b_g8t8")) == 9 + 15
     assert bench.launches_per_step(get_config("tiny_f32")) == 7
 
 

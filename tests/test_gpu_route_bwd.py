@@ -2,7 +2,9 @@
 inputs, one case per register-tile width of the CUDA kernels (rows of dl
 padded to 8, 16, 32, 64 and 72), with ragged token counts (not multiples of
 the 128-token tile) and hidden sizes that end inside a 64-column tile and a
-256-column tile. Outputs are fp32 sums of exactly representable inputs, so
+256-column tile, plus the tensor-core path (bf16, d a multiple of 256: dl as
+three bf16 planes through the grouped-GEMM kernels; with a dx_in addend the
+dx part stays on the CUDA cores). Outputs are fp32 sums of exactly representable inputs, so
 every case is held to the fp32 tolerance (relative Frobenius and max-abs
 1e-5)."""
 import dataclasses
@@ -25,6 +27,10 @@ CASES = [
     ("bf16", 1000, 520, 64, 8, False, True, False),  # 64 rows
     ("bf16", 129, 256, 64, 8, True, True, True),     # 65 rows -> 72
     ("f32", 77, 36, 5, 1, True, False, True),        # tiny, d not a multiple of 64
+    # bf16 with d % 256 == 0: the tensor-core path (dl split into three bf16 planes)
+    ("bf16", 1000, 512, 64, 8, False, True, False),  # 128-wide planes, dx GEMM
+    ("bf16", 3000, 768, 8, 2, True, True, False),    # gate row, 64-wide planes, dx GEMM
+    ("bf16", 2000, 256, 24, 4, False, False, False), # no renorm
 ]
 
 

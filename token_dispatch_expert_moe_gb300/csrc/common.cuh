@@ -212,4 +212,25 @@ struct RouteBwdArgs {
 size_t route_bwd_workspace_bytes(int64_t T, int d, int E);
 cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s);
 
+// Router backward on the tensor cores (bf16 layers, d % 256 == 0): dl split
+// into three bf16 planes (hi + mid + lo carries dl to ~fp32 precision) in
+// P [T, 4*PW] (plane k in columns [k*PW, k*PW + C), zeros elsewhere), and
+// Wr3 [3*PW, d] = W_r (+ w_sg row) repeated per plane.
+//   dW: out_w [nsplit, 4*PW, d] fp32 = P^T x per token chunk (weight-gradient
+//       GEMM with one group per chunk);
+//   dx: dx_router [T, d] fp32 = P[:, :3PW] Wr3 (dXp-mode GEMM, K = 3*PW),
+//       skipped when dx_router is NULL.
+struct RouterBwdTc {
+  int64_t T;
+  int d, PW;
+  const void *planes, *x, *Wr3;
+  float *out_w, *dx_router;   // out_w: [nsplit, 4*PW, d], one slice per token chunk
+  const int32_t *offs;  // [nsplit + 1] token-chunk boundaries, offs[0] = 0, offs[nsplit] = T;
+                        // offs[32..33] = {0, T} for the dx GEMM
+  int nsplit;
+  void *maps;           // 2 * nsplit tensor maps, 128-byte aligned
+  uint32_t *status;
+};
+cudaError_t launch_router_bwd_tc(const RouterBwdTc &a, cudaStream_t s);
+
 }  // namespace moe

@@ -1368,6 +1368,38 @@ cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   return launch_bn<DOWN>(q, s);
 }
 
+cudaError_t launch_router_bwd_tc(const RouterBwdTc &a, cudaStream_t s) {
+  const int PP = 4 * a.PW, d = a.d;
+  TcParams p{};
+  p.n_groups = 1; p.max_rows = a.T; p.d = d; p.offsets = a.offs; p.status = a.status;
+  cudaError_t e;
+  if (a.dx_router != nullptr) {  // dx = [hi | mid | lo] planes x Wr3, K = 3 PW
+    TcParams q = p;
+    q.offsets = a.offs + 32;   // one group of T rows
+    if (!make_map(&q.tmA, a.planes, PP, a.T, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.Wr3, d, 3 * (uint64_t)a.PW, 64)) return cudaErrorInvalidValue;
+    q.mode = DX; q.N = d; q.K_fixed = 3 * a.PW; q.b_group_rows = 3 * (int64_t)a.PW;
+    q.out0 = a.dx_router;
+    if (!make_store_map(&q.tmO0, a.dx_router, 4, d, a.T)) return cudaErrorInvalidValue;
+    if ((e = launch_bn<DX>(q, s)) != cudaSuccess) return e;
+  }
+  {  // dW: planes^T x, one group per token chunk
+    TcParams q = p;
+    q.n_groups = a.nsplit;
+    if (!make_map(&q.tmA, a.planes, PP, a.T, 64)) return cudaErrorInvalidValue;
+    if (!make_map(&q.tmB, a.x, d, a.T, 64)) return cudaErrorInvalidValue;
+    CUtensorMap *maps = static_cast<CUtensorMap *>(a.maps);
+    q.mode = WGD; q.M_fixed = PP; q.N = d; q.out0 = a.out_w; q.gmaps = maps;
+    if (!make_store_map(&q.tmO0, a.out_w, 4, d, (uint64_t)a.nsplit * PP)) return cudaErrorInvalidValue;
+    group_maps_kernel<<<1, 64, 0, s>>>(q.tmA, q.tmB, a.offs, a.nsplit, static_cast<const uint8_t *>(a.planes),
+                                       2 * (int64_t)PP, static_cast<const uint8_t *>(a.x), 2 * (int64_t)d,
+                                       a.T, maps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_bn<WGD>(q, s)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_ffn_bwd_bf16(const FfnArgs &a, cudaStream_t s) {
   const int d = a.d, F = a.F, E = a.n_groups;
   TcParams p{};

@@ -292,6 +292,71 @@ __global__ void reduce_kernel(RouteBwdArgs a, int nchunk) {
     a.dw_sg[j] = s;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core path (bf16 layers, d % 256 == 0). dl (fp32) is split exactly
+// enough into three bf16 planes: p1 = bf16(v), p2 = bf16(v - p1),
+// p3 = bf16(v - p1 - p2), so p1 + p2 + p3 equals v up to about 2^-24 |v|;
+// products of planes and bf16 weights or tokens are exact in the fp32
+// accumulators, so the GEMMs give the fp32 sums up to accumulation order.
+
+__global__ void __launch_bounds__(256) dl_planes_kernel(RouteBwdArgs a, __nv_bfloat16 *P, int PW,
+                                                        int32_t *offs, int nsplit) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i <= nsplit) offs[i] = (int32_t)(a.T * i / nsplit);   // token chunks of the dW_r GEMM
+  if (i < 2) offs[32 + i] = i == 0 ? 0 : (int32_t)a.T;      // the dx GEMM's single group
+  if (i >= a.T * PW) return;
+  const int64_t t = i / PW;
+  const int c = (int)(i - t * PW);
+  const int E = a.E;
+  float v = 0.0f;
+  if (c < E) v = a.dl[t * E + c];
+  else if (c == E && a.dz != nullptr) v = a.dz[t];
+  const __nv_bfloat16 p1 = __float2bfloat16_rn(v);
+  const float r1 = __fsub_rn(v, __bfloat162float(p1));
+  const __nv_bfloat16 p2 = __float2bfloat16_rn(r1);
+  const float r2 = __fsub_rn(r1, __bfloat162float(p2));
+  const __nv_bfloat16 p3 = __float2bfloat16_rn(r2);
+  __nv_bfloat16 *row = P + t * 4 * PW;
+  row[c] = p1;
+  row[PW + c] = p2;
+  row[2 * PW + c] = p3;
+  row[3 * PW + c] = __float2bfloat16_rn(0.0f);
+}
+
+// Wr3[k * PW + c] = W_r[c] (c < E), w_sg (c == E), 0 otherwise, k = 0, 1, 2.
+__global__ void __launch_bounds__(256) wr3_kernel(RouteBwdArgs a, __nv_bfloat16 *Wr3, int PW) {
+  const int64_t nvec = (int64_t)3 * PW * a.d / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= nvec) return;
+  const int64_t row = i * 8 / a.d;
+  const int j = (int)(i * 8 - row * a.d);
+  const int c = (int)(row % PW);
+  uint4 v = make_uint4(0, 0, 0, 0);
+  const __nv_bfloat16 *W = reinterpret_cast<const __nv_bfloat16 *>(a.W_r);
+  const __nv_bfloat16 *wsg = reinterpret_cast<const __nv_bfloat16 *>(a.w_sg);
+  if (c < a.E) v = *reinterpret_cast<const uint4 *>(W + (int64_t)c * a.d + j);
+  else if (c == a.E && wsg != nullptr) v = *reinterpret_cast<const uint4 *>(wsg + j);
+  *reinterpret_cast<uint4 *>(Wr3 + row * a.d + j) = v;
+}
+
+// dW_r[e] = sum over token chunks g, in order, of
+// (out[g][e] + out[g][PW + e]) + out[g][2 PW + e]; dw_sg from row E.
+__global__ void __launch_bounds__(256) plane_sum_kernel(RouteBwdArgs a, const float *out, int PW,
+                                                        int nsplit) {
+  const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)C * a.d) return;
+  const int c = (int)(i / a.d), j = (int)(i - (int64_t)c * a.d);
+  float v = 0.0f;
+  for (int g = 0; g < nsplit; ++g) {
+    const float *o = out + (int64_t)g * 4 * PW * a.d;
+    v = __fadd_rn(v, __fadd_rn(__fadd_rn(o[(int64_t)c * a.d + j], o[(int64_t)(PW + c) * a.d + j]),
+                               o[(int64_t)(2 * PW + c) * a.d + j]));
+  }
+  if (c < a.E) a.dW_r[i] = v;
+  else a.dw_sg[j] = v;
+}
+
 __global__ void __launch_bounds__(1024) db_kernel(RouteBwdArgs a) {
   __shared__ float red[32];
   const int e = blockIdx.x;
@@ -303,9 +368,59 @@ __global__ void __launch_bounds__(1024) db_kernel(RouteBwdArgs a) {
 
 }  // namespace
 
+constexpr size_t align256_(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Plane width of the tensor-core path: the C = E (+1 with the shared-expert
+// gate) dl columns padded to a multiple of 64 (one 64-deep K block of the dx
+// GEMM per plane).
+int tc_plane_width(int C) { return C <= 64 ? 64 : 128; }
+
+struct TcLayout {
+  size_t planes, wr3, out, offs, maps, total;
+};
+// The dW_r GEMM reduces over the T tokens; one group would give few, very
+// long tiles, so the tokens are cut into up to kMaxSplit chunks (groups of
+// the weight-gradient GEMM) and plane_sum_kernel adds the chunks in order.
+constexpr int kMaxSplit = 16;
+
+TcLayout tc_layout(int64_t T, int d, int PW) {
+  TcLayout L{};
+  size_t off = 0;
+  L.planes = off; off += align256_((size_t)T * 4 * PW * 2);
+  L.wr3 = off;    off += align256_((size_t)3 * PW * d * 2);
+  L.out = off;    off += align256_((size_t)kMaxSplit * 4 * PW * d * 4);
+  L.offs = off;   off += 256;
+  L.maps = off;   off += align256_((size_t)2 * kMaxSplit * 128);   // tensor maps
+  L.total = off + 256;          // room to align the region's start to 256 bytes
+  return L;
+}
+
 size_t route_bwd_workspace_bytes(int64_t T, int d, int E) {
-  const size_t dl = ((size_t)T * E * sizeof(float) + 255) & ~size_t(255);
-  return dl + (size_t)kChunks * (E + 1) * d * sizeof(float);
+  const size_t dl = align256_((size_t)T * E * sizeof(float));
+  const size_t cuda_path = (size_t)kChunks * (E + 1) * d * sizeof(float);
+  const size_t tc_path = tc_layout(T, d, tc_plane_width(E + 1)).total;   // the widest planes
+  return dl + (cuda_path > tc_path ? cuda_path : tc_path);
+}
+
+template <typename T, int CP>
+void launch_dx_t(const RouteBwdArgs &a, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ttiles = (int)((a.T + kDxT - 1) / kDxT), jtiles = (a.d + kDxJ - 1) / kDxJ;
+  int ysplit = (2 * (sms > 0 ? sms : 148) + ttiles - 1) / ttiles;
+  ysplit = ysplit < 1 ? 1 : (ysplit > jtiles ? jtiles : ysplit);
+  const int nsub = (jtiles + ysplit - 1) / ysplit;
+  dim3 gdx((unsigned)ttiles, (unsigned)((jtiles + nsub - 1) / nsub));
+  auto k = dx_kernel<T, CP>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dx_smem_bytes<CP>());
+  k<<<gdx, 256, dx_smem_bytes<CP>(), s>>>(a, nsub);
+}
+
+template <int CP>
+void launch_dx(const RouteBwdArgs &a, cudaStream_t s) {
+  if (a.dtype == MOE_BF16) launch_dx_t<__nv_bfloat16, CP>(a, s);
+  else launch_dx_t<float, CP>(a, s);
 }
 
 template <typename T, int CP>
@@ -334,6 +449,52 @@ void launch_cp(const RouteBwdArgs &a, cudaStream_t s, int64_t chunk, int nchunk)
 
 cudaError_t launch_route_bwd(const RouteBwdArgs &a, cudaStream_t s) {
   dl_kernel<<<(unsigned)((a.T * 32 + 255) / 256), 256, 0, s>>>(a);
+  if (a.dtype == MOE_BF16 && a.d % 256 == 0 && a.T < (int64_t(1) << 31) / 512) {
+    // tensor cores: dl planes, then the two GEMMs (dx on the CUDA cores when
+    // a dx_in has to be added, which the GEMM epilogue does not do)
+    const int PW = tc_plane_width(a.E + (a.w_sg != nullptr ? 1 : 0));
+    const TcLayout L = tc_layout(a.T, a.d, PW);
+    // the region the CUDA path uses for partials, its start aligned to 256 bytes
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(a.partial) + 255) & ~uintptr_t(255));
+    RouterBwdTc r{};
+    r.T = a.T; r.d = a.d; r.PW = PW; r.x = a.x; r.status = a.status;
+    __nv_bfloat16 *P = reinterpret_cast<__nv_bfloat16 *>(base + L.planes);
+    __nv_bfloat16 *Wr3 = reinterpret_cast<__nv_bfloat16 *>(base + L.wr3);
+    int32_t *offs = reinterpret_cast<int32_t *>(base + L.offs);
+    r.planes = P; r.Wr3 = Wr3; r.offs = offs; r.maps = base + L.maps;
+    r.out_w = reinterpret_cast<float *>(base + L.out);
+    r.dx_router = a.dx_in == nullptr ? a.dx_router : nullptr;
+    // token chunks: about one pair tile per cluster (4 PW / 256 M tiles x d / 256 N tiles each)
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tiles = (4 * PW / 256) * (a.d / 256);
+    int nsplit = ((sms > 0 ? sms : 148) + tiles - 1) / tiles;
+    nsplit = nsplit < 1 ? 1 : (nsplit > kMaxSplit ? kMaxSplit : nsplit);
+    if (a.T < (int64_t)nsplit * 64) nsplit = 1;
+    r.nsplit = nsplit;
+    const int64_t np = a.T * PW;
+    dl_planes_kernel<<<(unsigned)((np + 255) / 256), 256, 0, s>>>(a, P, PW, offs, nsplit);
+    if (r.dx_router != nullptr) {
+      const int64_t nv = (int64_t)3 * PW * a.d / 8;
+      wr3_kernel<<<(unsigned)((nv + 255) / 256), 256, 0, s>>>(a, Wr3, PW);
+    } else {   // CUDA-core dx with the dx_in addend
+      const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
+      if (C <= 8) launch_dx<8>(a, s);
+      else if (C <= 16) launch_dx<16>(a, s);
+      else if (C <= 32) launch_dx<32>(a, s);
+      else if (C <= 64) launch_dx<64>(a, s);
+      else launch_dx<72>(a, s);
+    }
+    cudaError_t e = launch_router_bwd_tc(r, s);
+    if (e != cudaSuccess) return e;
+    const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
+    const int64_t n = (int64_t)C * a.d;
+    plane_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, r.out_w, PW, nsplit);
+    if (a.db_r != nullptr) db_kernel<<<a.E, 1024, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t chunk = (a.T + kChunks - 1) / kChunks;
   const int nchunk = (int)((a.T + chunk - 1) / chunk);
   const int C = a.E + (a.w_sg != nullptr ? 1 : 0);
