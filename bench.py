@@ -181,6 +181,17 @@ def code_text(path: str) -> str:
     return "\n".join(out)
 
 
+def route_algorithmic_bytes(cfg) -> int:
+    """HBM bytes moe_route must move: x and the router weights (and the gate
+    vector) read once; logits (and gate logits) written; Top-K index, prob,
+    weight and keep flag written per slot."""
+    b = 2 if cfg.dtype == "bf16" else 4
+    n = cfg.T * cfg.d * b + cfg.E * cfg.d * b + cfg.T * cfg.E * 4
+    if cfg.Fs:
+        n += cfg.d * b + cfg.T * 4
+    return n + cfg.T * cfg.K * (4 + 4 + 4 + 1)
+
+
 def launches_per_step(cfg, etp: int = 1) -> int:
     bf16 = cfg.dtype == "bf16"
     n = 2 if bf16 else 1                   # router: logits GEMM + Top-K (fp32: one fused kernel)
@@ -287,14 +298,16 @@ def main():
     dout = to_device(inp["dout"]) if cfg.backward else None
     stream = torch.cuda.current_stream()
 
-    ffn_ev, perm_ev, unperm_ev, ffn_bwd_ev = [], [], [], []
+    ffn_ev, perm_ev, unperm_ev, ffn_bwd_ev, route_ev = [], [], [], [], []
 
     def step(x, out, record=False):
         c, s, ws = cfg_r, layer.shape, layer.ws
         layer.x = x
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(8)] if record else None
+        if record: e[6].record(stream)
         L.moe_route(s, x, w["W_r"], w.get("b_r"), w.get("w_sg"), layer.logits, layer.gate_logit,
                     layer.topk_idx, layer.topk_prob, layer.topk_w, layer.keep, ws)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if record else None
+        if record: e[7].record(stream)
         if record: e[0].record(stream)
         permute = L.moe_permute_padded if args.layout == "padded" else L.moe_permute
         permute(s, x, layer.topk_idx, layer.keep, layer.Xp, layer.row_of, layer.src_of,
@@ -318,6 +331,7 @@ def main():
             perm_ev.append((e[0], e[1]))
             ffn_ev.append((e[2], e[3]))
             unperm_ev.append((e[4], e[5]))
+            route_ev.append((e[6], e[7]))
 
     for _ in range(args.warmup):
         step(x, layer.out)
@@ -346,6 +360,9 @@ def main():
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ffn_ev)
     perm_ms = statistics.mean(a.elapsed_time(b) for a, b in perm_ev)
     unperm_ms = statistics.mean(a.elapsed_time(b) for a, b in unperm_ev)
+    # the stream is idle when the timed region starts, so the first step's
+    # route also waits for the host's launches: average the later steps
+    route_ms = statistics.mean(a.elapsed_time(b) for a, b in (route_ev[1:] or route_ev))
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk_path):
@@ -358,6 +375,7 @@ def main():
     b = 2 if cfg.dtype == "bf16" else 4
     perm_bytes = cfg.T * cfg.d * b + n_kept * cfg.d * b + cfg.T * cfg.K * 9
     unperm_bytes = n_kept * cfg.d * b + cfg.T * cfg.d * b + cfg.T * cfg.K * 8
+    route_bytes = route_algorithmic_bytes(cfg)
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
@@ -446,6 +464,8 @@ def main():
                 "permute_hbm_frac": perm_bytes / perm_ms / 1e6 / hbm_peak,
                 "unpermute_ms": unperm_ms, "unpermute_GBps": unperm_bytes / unperm_ms / 1e6,
                 "unpermute_hbm_frac": unperm_bytes / unperm_ms / 1e6 / hbm_peak,
+                "route_ms": route_ms, "route_GBps": route_bytes / route_ms / 1e6,
+                "route_hbm_frac": route_bytes / route_ms / 1e6 / hbm_peak,
                 "hbm_peak_GBps": hbm_peak,
             },
         }

@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* bad pointer, size or alignment                    */
-  MOE_ERR_UNSUPPORTED = 2, /* valid, but a shape this build has no kernel for   */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but a shape the library has no kernel for */
   MOE_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed               */
   MOE_ERR_TIMEOUT = 4,     /* device: a bounded wait gave up (status word only)  */
   MOE_ERR_DEVICE = 5       /* device: an index check failed (status word only)   */
@@ -99,7 +99,11 @@ moe_status_t moe_get_status(void *ws, moe_stream_t stream, uint32_t *info);
  * section 3.3 (sub-sequence dropping is the default drop rule).
  *   x [T,d] dtype; W_r [E,d] dtype; b_r [E] fp32 or NULL (added to logits);
  *   w_sg [d] dtype or NULL: shared-expert gate vector;
- *   out: logits [T,E] fp32 = x W_r^T (+ b_r), accumulated in fp32;
+ *   out: logits [T,E] fp32 = x W_r^T (+ b_r), accumulated in fp32 (bf16
+ *        with d % 64 == 0: on the tensor cores, the K loop split in up to
+ *        four fixed parts when the token count leaves SMs idle; the parts'
+ *        fp32 sums are added in order, so the result is the same on every
+ *        run on one GPU model);
  *        gate_logit [T] fp32 = x . w_sg (NULL iff w_sg is NULL);
  *        topk_idx [T,K] int32, topk_prob [T,K] fp32, topk_w [T,K] fp32,
  *        keep [T,K] uint8: as moe_route_topk.

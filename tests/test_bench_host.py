@@ -71,3 +71,16 @@ def test_traffic_key_ignores_comments_only(tmp_path):
     assert bench.code_text(str(a)) == bench.code_text(str(b))
     assert bench.code_text(str(a)) != bench.code_text(str(c))
 
+
+
+def test_route_bytes():
+    import bench
+    from synthetic import get_config
+    # Mixtral-8x22B shape: x 8192 x 6144 bf16, W_r 8 x 6144 bf16, logits
+    # 8192 x 8 fp32, 8192 x 2 slots of (index, prob, weight, keep)
+    assert bench.route_algorithmic_bytes(get_config("mixtral_8x22b")) == (
+        100663296 + 98304 + 262144 + 212992)
+    # Qwen2 shape adds the gate vector (3584 bf16) and 8192 fp32 gate logits
+    q = get_config("qwen2_57b_a14b")
+    assert bench.route_algorithmic_bytes(q) == (
+        8192 * 3584 * 2 + 64 * 3584 * 2 + 8192 * 64 * 4 + 3584 * 2 + 8192 * 4 + 8192 * 8 * 13)

@@ -52,12 +52,16 @@ def test_route_topk_bit_exact(name, ties):
     _assert_same_decisions(g, r)
 
 
-@pytest.mark.parametrize("variant", ["full_seq_drop", "no_renorm", "ragged_subseq", "k1", "e64k8_cf"])
+@pytest.mark.parametrize("variant", ["full_seq_drop", "no_renorm", "ragged_subseq", "k1", "e64k8_cf",
+                                     "full_seq_drop_global_keys"])
 def test_route_topk_variants(variant):
     L = lib()
     base = get_config("mixtral_8x22b_g8t8@small")
     cfg = {
         "full_seq_drop": dataclasses.replace(base, S=0),
+        # a sub-sequence longer than the capacity kernel's shared-memory key
+        # buffer (16384 candidates): the keys go to the workspace
+        "full_seq_drop_global_keys": dataclasses.replace(base, T=20000, S=0),
         "no_renorm": dataclasses.replace(base, renorm=False),
         "ragged_subseq": dataclasses.replace(base, T=1000, S=300),
         "k1": dataclasses.replace(base, K=1, E=16, cf=0.5),
@@ -83,8 +87,27 @@ def test_exp_and_softmax_bits_over_a_wide_range():
 
 @pytest.mark.parametrize("name", SMALL + FULL)
 def test_route_fused(name):
+    _check_route(get_config(name))
+
+
+# bf16 shapes whose row tiles (T / 128) leave SMs idle, so the tensor-core
+# logits split their K loop: 4 splits of 8 K blocks (gate logit and bias
+# ride along), 3 splits over 3 ragged row tiles, 2 splits of 8 K blocks
+SPLIT_K = {
+    "split4_gate_bias": ("qwen2_57b_a14b", dict(T=1000, d=2048, F=128, Fs=128)),
+    "split3_ragged": ("mixtral_8x22b", dict(T=300, d=1536, F=128, S=100)),
+    "split2_e64": ("mixtral_8x22b_g8t8", dict(T=2000, d=1024, F=128, S=500)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SPLIT_K))
+def test_route_split_k(case):
+    base, kw = SPLIT_K[case]
+    _check_route(dataclasses.replace(get_config(base), name=f"{base}@{case}", **kw))
+
+
+def _check_route(cfg):
     L = lib()
-    cfg = get_config(name)
     inp = inputs(cfg, need_backward=False)
     T, E, K = cfg.T, cfg.E, cfg.K
     s = L.shape_of(cfg)

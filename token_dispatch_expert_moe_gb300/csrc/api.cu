@@ -31,8 +31,13 @@ int64_t subseq(const moe_shape_t *s) {
 }
 
 struct Layout {
-  size_t status, map, cap, rbwd, total;
+  size_t status, map, cap, rbwd, rpart, total;
 };
+
+// the tensor-core router's logits path (bf16, d % 64 == 0)
+bool router_on_tensor_cores(const moe_shape_t *s) {
+  return s->dtype == MOE_BF16 && s->d % 64 == 0;
+}
 
 Layout layout(const moe_shape_t *s) {
   Layout L{};
@@ -48,6 +53,9 @@ Layout layout(const moe_shape_t *s) {
   }
   L.rbwd = off;
   off += align256(route_bwd_workspace_bytes(s->T, s->d, s->E));
+  L.rpart = off;   // the router GEMM's K-split partial sums (any split count)
+  if (router_on_tensor_cores(s))
+    off += align256((size_t)kRouterMaxSplit * s->T * (s->E + 1) * sizeof(float));
   L.total = off > MOE_FFN_BWD_WORKSPACE_BYTES ? off : MOE_FFN_BWD_WORKSPACE_BYTES;
   return L;
 }
@@ -117,8 +125,11 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
   a.topk_idx = topk_idx; a.topk_prob = topk_prob; a.topk_w = topk_w; a.keep = keep;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  if (shape->dtype == MOE_BF16 && shape->d % 64 == 0 && (w_sg == nullptr || aligned16(w_sg))) {
+  if (router_on_tensor_cores(shape) && (w_sg == nullptr || aligned16(w_sg))) {
     // logits on the tensor cores, then the fp32 Top-K on those logits
+    a.rt_split = router_k_split(shape->T, shape->d);
+    if (a.rt_split > 1)
+      a.rt_part = reinterpret_cast<float *>(static_cast<char *>(ws) + layout(shape).rpart);
     e = launch_router_tc(a, s);
     if (e == cudaSuccess) e = launch_topk_from_logits(a, s);
   } else {

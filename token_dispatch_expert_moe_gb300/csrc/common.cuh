@@ -129,7 +129,16 @@ struct RouteArgs {
   uint32_t *status;
   unsigned long long *cap_keys;  // ws region for capacity candidates
   uint32_t *cap_count;           // ws region, one counter per (sub-seq, expert)
+  // tensor-core logits with a split K loop: rt_split partial sums
+  // [rt_split][T][E + (w_sg != null)] that the Top-K kernel adds in split order
+  int rt_split;                  // <= 1: no split (logits written directly)
+  float *rt_part;                // ws region
 };
+
+constexpr int kRouterMaxSplit = 4;
+// K splits of the router GEMM for T tokens of hidden size d (d % 64 == 0):
+// as many as leave no SM idle, at most kRouterMaxSplit, >= 8 K blocks each
+int router_k_split(int64_t T, int d);
 
 cudaError_t launch_router_fused(const RouteArgs &a, cudaStream_t s);
 cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s);  // bf16, d % 64 == 0

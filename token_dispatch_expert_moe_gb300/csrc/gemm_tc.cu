@@ -33,7 +33,10 @@
 //   WGU     dW_gu[g]   = dA_g^T Xp_g
 //   RT      router logits = x W_r^T (+ b_r) and gate logit x . w_sg: one
 //           group of T rows, N = E rounded up to 16 (+ 16 when the gate
-//           vector rides along as a second B box); fp32 logits out.
+//           vector rides along as a second B box); fp32 logits out. When
+//           T / 128 row tiles would leave SMs idle, the K loop is split over
+//           k_split tiles per row tile whose fp32 partial sums the Top-K
+//           kernel adds in split order.
 // In GU/DOWN/DH/DX a tile's rows past the group's end belong to the next
 // group (or are zero-filled past the buffer); only their outputs are masked.
 // In WGD/WGU the reduction runs over the group's rows: the loads go through
@@ -97,6 +100,8 @@ struct TcParams {
   int E, e_pad, has_gate;
   const float *bias;
   float *gate_out;
+  int k_split, kb_per;  // K blocks split over k_split tiles of kb_per blocks each
+  float *part;          // k_split > 1: partial sums [k_split][T][E + has_gate]
   uint32_t *status;
 };
 
@@ -358,7 +363,8 @@ template <int MODE, int BN>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, const SharedState &st, int idx) {
   Tile t;
   if constexpr (MODE == RT) {
-    t.g = 0; t.n = 0; t.m = idx; t.row0 = 0; t.rows = (int)p.T;
+    t.g = 0; t.m = idx / p.k_split; t.n = idx % p.k_split;   // n: the K split
+    t.row0 = 0; t.rows = (int)p.T;
   } else if constexpr (ModeTraits<MODE>::red) {
     const int MT = p.M_fixed / BM, NT = p.N / BN;
     t.g = idx / (MT * NT);
@@ -408,7 +414,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
   if constexpr (MODE == RT) {
     const int64_t row = r_loc;
     const bool valid = row < p.T;
-    float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
+    const bool split = p.k_split > 1;
+    const int C = p.E + p.has_gate;
+    float *lg = split ? p.part + ((int64_t)t.n * p.T + row) * C
+                      : reinterpret_cast<float *>(p.out0) + row * p.E;
 #pragma unroll 1
     for (int c = 0; c < (BN + 31) / 32; ++c) {
       float v[32];
@@ -417,8 +426,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int e = c * 32 + i;
-          if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[i], p.bias[e]) : v[i];
-          if (p.has_gate && e == p.e_pad) p.gate_out[row] = v[i];
+          if (e < p.E) lg[e] = (!split && p.bias != nullptr) ? __fadd_rn(v[i], p.bias[e]) : v[i];
+          if (p.has_gate && e == p.e_pad) {
+            if (split) lg[p.E] = v[i];
+            else p.gate_out[row] = v[i];
+          }
         }
       }
     }
@@ -642,6 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
   constexpr uint32_t kStageTx = kABytes + MMA_N * BK * 2;
   constexpr uint32_t kIdesc = instr_desc(BM, MMA_N, TR::a_mn, TR::b_mn);
+  // the router's B operand is at most 80 rows (10 KB): six 32 KB stages in
+  // the space of four 48 KB ones keep more of x in flight
+  constexpr int NST = MODE == RT ? 6 : kStages;
+  constexpr int SBYTES = MODE == RT ? kABytes + 16384 : kStageBytes;
+  static_assert(NST * SBYTES <= kStages * kStageBytes && NST <= kMaxStages, "ring too large");
+  static_assert(MODE != RT || BN * BK * 2 <= 16384, "router B operand exceeds its stage");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -656,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int total = 0;
     bool bad = false;
     if constexpr (MODE == RT) {
-      total = (int)((p.T + BM - 1) / BM);
+      total = (int)((p.T + BM - 1) / BM) * p.k_split;
     } else if constexpr (TR::red) {
       for (int g = 0; g < p.n_groups; ++g)
         if (p.offsets[g + 1] < p.offsets[g]) bad = true;
@@ -681,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       total = 0;
     }
     st.total_tiles = total;
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&st.full[s]), 1);
       mbar_init(smem_u32(&st.empty[s]), 1);
     }
@@ -711,20 +729,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ======================= TMA producer =======================
     if (lane == 0 && !p.fault_stall) {
       int it = 0;
-      int last_phase[kStages];
+      int last_phase[NST];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+      for (int s = 0; s < NST; ++s) last_phase[s] = -1;
       for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x) {
         const Tile t = decode_tile<MODE, BN>(p, st, ti);
-        const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+        int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+        int kb0 = 0;   // first K block of the tile (the router's K split)
+        if constexpr (MODE == RT) {
+          kb0 = t.n * p.kb_per;
+          kblocks = min(p.kb_per, kblocks - kb0);
+        }
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1;
           if (!wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 1)) break;
           const uint32_t full = smem_u32(&st.full[s]);
           mbar_expect_tx(full, kStageTx);
           last_phase[s] = (int)ph;
-          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sa = smem_u32(smem + s * SBYTES);
           const uint32_t sb = sa + kABytes;
           if constexpr (TR::red) {   // K rows relative to the group's own maps
             const CUtensorMap *mA = p.gmaps + 2 * t.g, *mB = mA + 1;
@@ -740,11 +763,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               tma_load_2d(sb + b * 8192, mB, full, t.n * BN + 64 * b, kb * BK);
           } else {
             const int arow = t.row0 + t.m * BM;
-            tma_load_2d(sa, &p.tmA, full, kb * BK, arow);
+            tma_load_2d(sa, &p.tmA, full, (kb0 + kb) * BK, arow);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
             if constexpr (MODE == RT) {
-              tma_load_2d(sb, &p.tmB, full, kb * BK, 0);
-              if (p.has_gate) tma_load_2d(sb + p.e_pad * 128, &p.tmC, full, kb * BK, 0);
+              tma_load_2d(sb, &p.tmB, full, (kb0 + kb) * BK, 0);
+              if (p.has_gate) tma_load_2d(sb + p.e_pad * 128, &p.tmC, full, (kb0 + kb) * BK, 0);
             } else if constexpr (MODE == GU) {
               tma_load_2d(sb, &p.tmB, full, kb * BK, (int)(gb + t.n * 128));
               tma_load_2d(sb + 16384, &p.tmB, full, kb * BK, (int)(gb + p.F + t.n * 128));
@@ -761,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
       }
       // drain: every issued load must land before the CTA exits
-      for (int s = 0; s < kStages; ++s)
+      for (int s = 0; s < NST; ++s)
         if (last_phase[s] >= 0) {
           const uint32_t bar = smem_u32(&st.full[s]);
           const uint64_t t0 = globaltimer();
@@ -775,7 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     bool issued_any = false;
     for (int ti = blockIdx.x; ti < total && !st.abort; ti += gridDim.x, ++tcount) {
       const Tile t = decode_tile<MODE, BN>(p, st, ti);
-      const int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+      int kblocks = TR::red ? (t.rows + BK - 1) / BK : p.K_fixed / BK;
+      if constexpr (MODE == RT) kblocks = min(p.kb_per, kblocks - t.n * p.kb_per);
       const int buf = tcount & 1;
       const uint32_t use = (tcount >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2))) break;
@@ -783,14 +807,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const uint32_t dcol = tmem + buf * 256;
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int s = it % NST;
+        const uint32_t ph = (it / NST) & 1;
         if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint8_t *sa_p = smem + s * kStageBytes;
+        uint8_t *sa_p = smem + s * SBYTES;
         if (lane == 0) {
           const uint32_t sa = smem_u32(sa_p);
           const uint32_t sb = sa + kABytes;
@@ -1320,6 +1344,17 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
 
 }  // namespace
 
+int router_k_split(int64_t T, int d) {
+  const int64_t mtiles = (T + BM - 1) / BM;
+  const int kb = d / BK;
+  int64_t s = mtiles > 0 ? num_sms() / mtiles : 1;
+  if (s > kRouterMaxSplit) s = kRouterMaxSplit;
+  if (s > kb / 8) s = kb / 8;   // at least 8 K blocks per split
+  if (s < 1) s = 1;
+  const int per = (int)((kb + s - 1) / s);
+  return (kb + per - 1) / per;   // every split non-empty
+}
+
 cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
   const int e_pad = (a.E + 15) / 16 * 16;
   const int has_gate = a.w_sg != nullptr ? 1 : 0;
@@ -1331,6 +1366,12 @@ cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
   p.mode = RT; p.n_groups = 1; p.max_rows = a.T; p.d = a.d; p.K_fixed = a.d; p.N = n;
   p.T = a.T; p.E = a.E; p.e_pad = e_pad; p.has_gate = has_gate; p.bias = a.b_r;
   p.out0 = a.logits; p.gate_out = a.gate_logit; p.status = a.status;
+  const int kb = a.d / BK;
+  p.k_split = a.rt_split > 1 ? a.rt_split : 1;
+  p.kb_per = (kb + p.k_split - 1) / p.k_split;
+  if (p.k_split > 1 && (a.rt_part == nullptr || (p.k_split - 1) * p.kb_per >= kb))
+    return cudaErrorInvalidValue;
+  p.part = a.rt_part;
   switch (n) {
     case 16: return launch_mode<RT, 16>(p, s);
     case 32: return launch_mode<RT, 32>(p, s);

@@ -6,10 +6,12 @@
 // decided inside each sub-sequence; sub-sequence dropping is the default).
 //
 // bf16 layers compute the logits (and the shared-expert gate logit) on the
-// tensor cores (router mode of the grouped GEMM, gemm_tc.cu) and then run
-// topk_from_logits_kernel; fp32 layers use router_fused_kernel, which does
-// the logits GEMV, softmax and Top-K in one pass. capacity_kernel applies the
-// drop rule per (sub-sequence, expert). The softmax and Top-K arithmetic is
+// tensor cores (router mode of the grouped GEMM, gemm_tc.cu; with a split K
+// loop when T / 128 row tiles would leave SMs idle) and then run
+// topk_from_logits_kernel, which also adds the split partial sums and the
+// bias; fp32 layers use router_fused_kernel, which does the logits GEMV,
+// softmax and Top-K in one pass. capacity_kernel applies the drop rule per
+// (sub-sequence, expert). The softmax and Top-K arithmetic is
 // specified in softmax.cuh.
 #include "common.cuh"
 #include "softmax.cuh"
@@ -103,9 +105,37 @@ __global__ void __launch_bounds__(256) topk_from_logits_kernel(RouteArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= a.T) return;
-  const float *l = a.logits + t * a.E;
-  const float l0 = lane < a.E ? l[lane] : 0.0f;
-  const float l1 = lane + 32 < a.E ? l[lane + 32] : 0.0f;
+  float l0, l1;
+  if (a.rt_split > 1) {
+    // the router GEMM's K-split partial sums, added in split order, then the
+    // bias; the logits (and the gate logit) are written here
+    const int has_gate = a.gate_logit != nullptr ? 1 : 0;
+    const int C = a.E + has_gate;
+    float s0 = 0.0f, s1 = 0.0f, sg = 0.0f;
+    for (int k = 0; k < a.rt_split; ++k) {
+      const float *P = a.rt_part + ((int64_t)k * a.T + t) * C;
+      const float v0 = lane < a.E ? P[lane] : 0.0f;
+      const float v1 = lane + 32 < a.E ? P[lane + 32] : 0.0f;
+      const float vg = (has_gate && lane == 0) ? P[a.E] : 0.0f;
+      s0 = k == 0 ? v0 : __fadd_rn(s0, v0);
+      s1 = k == 0 ? v1 : __fadd_rn(s1, v1);
+      sg = k == 0 ? vg : __fadd_rn(sg, vg);
+    }
+    if (a.b_r != nullptr) {
+      if (lane < a.E) s0 = __fadd_rn(s0, a.b_r[lane]);
+      if (lane + 32 < a.E) s1 = __fadd_rn(s1, a.b_r[lane + 32]);
+    }
+    float *l = a.logits + t * a.E;
+    if (lane < a.E) l[lane] = s0;
+    if (lane + 32 < a.E) l[lane + 32] = s1;
+    if (has_gate && lane == 0) a.gate_logit[t] = sg;
+    l0 = lane < a.E ? s0 : 0.0f;
+    l1 = lane + 32 < a.E ? s1 : 0.0f;
+  } else {
+    const float *l = a.logits + t * a.E;
+    l0 = lane < a.E ? l[lane] : 0.0f;
+    l1 = lane + 32 < a.E ? l[lane + 32] : 0.0f;
+  }
   spec::softmax_topk_warp(l0, l1, a.E, a.K, a.renorm, a.topk_idx + t * a.K, a.topk_prob + t * a.K,
                     a.topk_w + t * a.K, a.keep + t * a.K);
 }
@@ -115,7 +145,10 @@ __global__ void __launch_bounds__(256) topk_from_logits_kernel(RouteArgs a) {
 // the assignments (t, k) of the sub-sequence routed to e, keyed by
 // (fp32 bits of p) << 32 | (2^32 - 1 - t): a larger key is a higher
 // probability, then a lower token index. Keys are unique, so the cap largest
-// are found exactly by an 8-pass MSB radix select of the cap-th largest key.
+// are found exactly by an MSB radix select (8-bit digits) of the cap-th
+// largest key. The select stops at the first digit whose bin is kept whole:
+// the threshold is then that bin's prefix with zero low bits, which every key
+// of the bin reaches and no key of a lower bin does.
 constexpr int kCapThreads = 512;
 constexpr int kCapSmemKeys = 16384;   // candidates kept in shared memory (128 KB)
 
@@ -126,6 +159,7 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long sh_prefix;
   __shared__ uint32_t sh_need;
+  __shared__ int sh_done;
   const int j = blockIdx.x, e = blockIdx.y;
   const int64_t lo = (int64_t)j * a.S;
   const int64_t hi = min(a.T, lo + a.S);
@@ -136,12 +170,21 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) n_cand = 0;
   __syncthreads();
-  for (int64_t t = lo + threadIdx.x; t < hi; t += blockDim.x) {
+  // candidates: one shared-memory atomic per warp and slot
+  const uint32_t lanes_below = (1u << lane) - 1u;
+  for (int64_t t0 = lo; t0 < hi; t0 += blockDim.x) {
+    const int64_t t = t0 + threadIdx.x;
     for (int k = 0; k < K; ++k) {
-      if (a.topk_idx[t * K + k] == e) {
-        const uint32_t pos = atomicAdd(&n_cand, 1u);
+      const bool m = t < hi && a.topk_idx[t * K + k] == e;
+      const uint32_t ballot = __ballot_sync(0xffffffffu, m);
+      if (ballot == 0u) continue;
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (m) {
         const uint32_t pbits = __float_as_uint(a.topk_prob[t * K + k]);
-        keys[pos] = ((unsigned long long)pbits << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
+        keys[base + __popc(ballot & lanes_below)] =
+            ((unsigned long long)pbits << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
       }
     }
   }
@@ -149,7 +192,7 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
   const uint32_t n = n_cand;
   unsigned long long threshold = 0;
   if (n > (uint32_t)cap) {
-    if (threadIdx.x == 0) { sh_prefix = 0; sh_need = (uint32_t)cap; }
+    if (threadIdx.x == 0) { sh_prefix = 0; sh_need = (uint32_t)cap; sh_done = 0; }
     for (int shift = 56; shift >= 0; shift -= 8) {
       for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
       __syncthreads();
@@ -179,18 +222,20 @@ capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
         const uint32_t need = sh_need;
         const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
         if (lane == __ffs(hit) - 1) {
-          uint32_t cum = excl;
+          uint32_t cum = excl, cnt = 0;
           int digit = 0;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            if (cum + c[i] >= need) { digit = 255 - 8 * lane - i; break; }
+            if (cum + c[i] >= need) { digit = 255 - 8 * lane - i; cnt = c[i]; break; }
             cum += c[i];
           }
           sh_need = need - cum;
           sh_prefix = pre | ((unsigned long long)digit << shift);
+          sh_done = (need - cum == cnt) ? 1 : 0;   // the digit's whole bin is kept
         }
       }
       __syncthreads();
+      if (sh_done) break;
     }
     threshold = sh_prefix;
   }
