@@ -93,6 +93,28 @@ def test_capacity_brute_force(T, E, K, S, cf, ties):
     assert np.array_equal(keep, _brute_keep(idx, prob, E, cf, S))
 
 
+def test_capacity_short_last_subsequence_uses_its_own_length():
+    """T = 37 in sub-sequences of 16 leaves a last one of 5 tokens, whose
+    capacity is ceil(1.0 * 5 * 2 / 4) = 3 (the full blocks' is 8). Expert 0
+    is every token's first choice, so it has 5 candidates there and keeps 3,
+    the 3 highest-probability ones."""
+    rng = np.random.default_rng(11)
+    T, E, K, S = 37, 4, 2, 16
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[:, 0] += np.float32(6.0)
+    p = O.softmax_f32(l)
+    idx, prob = O.topk(p, K)
+    keep = O.capacity_keep(idx, prob, E, 1.0, S)
+    assert np.array_equal(keep, _brute_keep(idx, prob, E, 1.0, S))
+    last = slice(32, 37)
+    assert np.all(idx[last, 0] == 0)
+    kept = keep[last, 0]
+    assert kept.sum() == 3
+    assert prob[last, 0][kept == 1].min() > prob[last, 0][kept == 0].max()
+    for lo in (0, 16):   # full blocks: 16 candidates, 8 kept
+        assert keep[lo:lo + 16, 0].sum() == 8
+
+
 def test_capacity_invariants():
     rng = np.random.default_rng(5)
     T, E, K, S = 1000, 8, 2, 256
