@@ -58,8 +58,10 @@ typedef void *moe_stream_t; /* a cudaStream_t */
  * Top-K gating and the capacity factor; "method overview" and "key modules":
  * drop and dropless routing, sub-sequence dropping).                          */
 typedef struct {
-  int64_t T;               /* tokens (micro-batch x sequence, flattened)      */
-  int32_t d;               /* hidden size                                    */
+  int64_t T;               /* tokens (micro-batch x sequence, flattened),
+                              >= 1 and T * K < 2^31 (an empty batch is an
+                              invalid shape: the caller skips the layer)     */
+  int32_t d;               /* hidden size, a multiple of 8 (bf16) or 4 (fp32) */
   int32_t E;               /* routed experts, 1..64                          */
   int32_t K;               /* Top-K, 1..min(E, 8)                            */
   int32_t F;               /* routed expert SwiGLU intermediate size         */
