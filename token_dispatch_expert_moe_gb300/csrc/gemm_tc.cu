@@ -16,8 +16,8 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
 //               quarter per warp), fused math, 32-row slabs staged in swizzled
 //               shared memory and written with TMA bulk stores.
-// tc_gemm_kernel: one CTA per tile, M = 128, 4 stages of 48 KB (used by the
-// router GEMM and when CTA pairs are disabled). tc_gemm_pair_kernel: clusters
+// tc_gemm_kernel: one CTA per tile, M = 128, 4 stages of 48 KB (6 of 32 KB in
+// the router mode; used by the router GEMM and when CTA pairs are disabled). tc_gemm_pair_kernel: clusters
 // of two CTAs on one TPC issue tcgen05.mma.cta_group::2 (M = 256, each CTA
 // holding its 128 rows of A and half of B), 6 stages of 32 KB per CTA; the
 // even CTA's barriers see both CTAs' TMA bytes and its MMA warp issues for the
