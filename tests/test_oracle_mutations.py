@@ -16,7 +16,7 @@ from tests import test_oracle_softmax as PS
 
 _orig = {n: getattr(O, n) for n in (
     "silu", "swiglu_group", "route_bwd", "sigmoid", "capacity", "unpermute", "unpermute_bwd",
-    "permute_bwd", "sum_partials", "router_logits", "padded_capacity")}
+    "permute_bwd", "sum_partials", "router_logits", "padded_capacity", "route")}
 
 
 # ---- mutants ----
@@ -122,6 +122,14 @@ def _build_map_tokens_descending(idx, keep, E):
     return counts, offsets, row_of, (t * K + k).astype(np.int32), n_kept
 
 
+def _route_ranks_capacity_by_weight(cfg, inp, mirror=True, logits=None):
+    """route() with the capacity keys taken from the renormalised weights."""
+    r = _orig["route"](cfg, inp, mirror=mirror, logits=logits)
+    if cfg.drop:
+        r["keep"] = O.capacity_keep(r["topk_idx"], r["topk_w"], cfg.E, cfg.cf, cfg.subseq)
+    return r
+
+
 def _pairwise_sum_sequential(q):
     q = np.asarray(q, dtype=np.float32)
     acc = np.zeros(q.shape[:-1], dtype=np.float32)
@@ -195,6 +203,8 @@ MUTANTS = {
     "capacity: short last sub-sequence gets the full cap": (
         {"capacity_keep": _capacity_keep(full_cap_for_short_block=True)},
         PR.test_capacity_short_last_subsequence_uses_its_own_length),
+    "capacity ranked by the renormalised weight": (
+        {"route": _route_ranks_capacity_by_weight}, PR.test_route_composes_the_pinned_steps),
     "map: tokens descending inside an expert": (
         {"build_map": _build_map_tokens_descending}, lambda: PR.test_map_invariants(False)),
     "padded capacity not clipped to the sub-sequence": (

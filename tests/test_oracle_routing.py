@@ -167,6 +167,37 @@ def test_map_invariants(drop):
         assert np.all(np.diff(t_of[seg]) > 0)
 
 
+def test_route_composes_the_pinned_steps():
+    """route() wires the steps the way the readings say: Top-K on the fp32
+    softmax of the logits; capacity ranks by the raw probability p (not the
+    renormalised weight); the weights are prob / (sum of the K probs); a
+    dropless layer keeps every slot."""
+    from synthetic import MoEConfig
+    rng = np.random.default_rng(21)
+    for drop, renorm, K, cf in [(True, True, 2, 0.6), (True, False, 3, 0.5), (False, True, 2, 1.0)]:
+        cfg = MoEConfig("r", T=48, d=8, E=6, K=K, F=8, dtype="f32", drop=drop, cf=cf, S=16,
+                        renorm=renorm)
+        logits = (rng.standard_normal((cfg.T, cfg.E)) * 2).astype(np.float32)
+        r = O.route(cfg, None, logits=logits.astype(np.float64))
+        p = O.softmax_f32(logits)
+        assert np.array_equal(r["p"], p)
+        for t in range(cfg.T):   # Top-K by the brute-force total order
+            for k in range(K - 1):
+                assert _beats(p[t], r["topk_idx"][t, k], r["topk_idx"][t, k + 1])
+            rest = [e for e in range(cfg.E) if e not in r["topk_idx"][t]]
+            assert all(_beats(p[t], r["topk_idx"][t, K - 1], e) for e in rest)
+        prob = np.take_along_axis(p, r["topk_idx"].astype(np.int64), axis=1)
+        assert np.array_equal(r["topk_prob"], prob)
+        w_ref = prob / prob.sum(axis=1, keepdims=True, dtype=np.float32) if renorm else prob
+        assert np.allclose(r["topk_w"], w_ref, rtol=2e-7, atol=0)
+        if drop:
+            keep = _brute_keep(r["topk_idx"], prob, cfg.E, cf, cfg.S)
+            assert 0 < keep.sum() < cfg.T * K
+        else:
+            keep = np.ones((cfg.T, K), np.uint8)
+        assert np.array_equal(r["keep"], keep)
+
+
 # ---- GShard-style padded layout (f2) ----
 
 def test_padded_map_is_the_compact_map_with_fixed_strides():
