@@ -16,7 +16,7 @@ from tests import test_oracle_softmax as PS
 
 _orig = {n: getattr(O, n) for n in (
     "silu", "swiglu_group", "route_bwd", "sigmoid", "capacity", "unpermute", "unpermute_bwd",
-    "permute_bwd", "sum_partials", "router_logits", "padded_capacity", "route")}
+    "permute_bwd", "sum_partials", "router_logits", "padded_capacity", "route", "expert_ffn")}
 
 
 # ---- mutants ----
@@ -130,6 +130,26 @@ def _route_ranks_capacity_by_weight(cfg, inp, mirror=True, logits=None):
     return r
 
 
+def _expert_rows_one_late(Xp, offsets, W_gu, W_down, dtype="bf16", mirror=True, rows=None):
+    off = np.array(offsets, copy=True)
+    off[:-1] = np.minimum(off[:-1] + 1, off[1:])
+    return _orig["expert_ffn"](Xp, off, W_gu, W_down, dtype, mirror, rows)
+
+
+def _unpermute_bwd_dw_from_next_slot(dout, Yp, row_of, w, *a, **k):
+    """dw[t, k] = <dout[t], Yp[row_of[t, k + 1]]>: an off-by-one slot index."""
+    r = _orig["unpermute_bwd"](dout, Yp, row_of, w, *a, **k)
+    r["dw"] = _orig["unpermute_bwd"](dout, Yp, np.roll(row_of, -1, axis=1), w, *a, **k)["dw"]
+    return r
+
+
+def _softmax_without_max(logits):
+    l = np.asarray(logits, dtype=np.float32)
+    q = O.exp_f32(l)
+    s = O.pairwise_sum_f32(q)[..., None]
+    return (q / s).astype(np.float32)
+
+
 def _pairwise_sum_sequential(q):
     q = np.asarray(q, dtype=np.float32)
     acc = np.zeros(q.shape[:-1], dtype=np.float32)
@@ -214,6 +234,13 @@ MUTANTS = {
     "exp: polynomial truncated after r^5": (
         {"TAYLOR": O.TAYLOR[:6] + [np.float32(0.0), np.float32(0.0)]},
         PS.test_exp_within_two_ulp_of_double_exp),
+    "expert rows start one row late": (
+        {"expert_ffn": _expert_rows_one_late}, PL.test_single_expert_is_dense_swiglu),
+    "un-permute backward: dw from the neighbouring slot's row": (
+        {"unpermute_bwd": _unpermute_bwd_dw_from_next_slot},
+        lambda: PL.test_backward_matches_finite_differences("no_renorm")),
+    "softmax without the max subtraction": (
+        {"softmax_f32": _softmax_without_max}, PS.test_softmax_bits_invariant_under_a_shift_of_the_logits),
     "softmax sum left to right": (
         {"pairwise_sum_f32": _pairwise_sum_sequential}, PS.test_pairwise_sum_order),
     "ETP shard: gate rows used for up": (
@@ -225,6 +252,7 @@ MUTANTS = {
 }
 
 
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")   # mutants may overflow
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pin_catches_planted_mistake(name, monkeypatch):
     patches, pin = MUTANTS[name]

@@ -108,3 +108,18 @@ def test_softmax_close_to_exact_and_normalised(E):
     assert np.all(np.abs(p.sum(axis=1) - 1.0) <= E * 2.0**-23)
     # the largest logit gets the largest probability
     assert np.array_equal(np.argmax(p, axis=1), np.argmax(l, axis=1))
+
+
+def test_softmax_bits_invariant_under_a_shift_of_the_logits():
+    """softmax(l + c) = softmax(l). With logits on a 2^-10 grid and |l| < 32,
+    l + c is exact in fp32 for c = 96 and c = 1000, and so is l + c - max; the
+    specified arithmetic (subtract the row maximum first) therefore gives the
+    same bits. Without the max subtraction e^(l + c) leaves the fp32 range."""
+    rng = np.random.default_rng(5)
+    l = np.clip(np.round(rng.standard_normal((2000, 8)) * 3 * 1024) / 1024, -31, 31)
+    l = l.astype(np.float32)
+    p = O.softmax_f32(l)
+    for c in (96.0, 1000.0):
+        lc = (l + np.float32(c)).astype(np.float32)
+        assert np.array_equal(lc.astype(np.float64) - c, l.astype(np.float64))   # exact shift
+        assert np.array_equal(O.softmax_f32(lc).view(np.uint32), p.view(np.uint32))
