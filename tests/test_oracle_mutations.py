@@ -13,6 +13,7 @@ from oracle import moe_oracle as O
 from tests import test_oracle_layer as PL
 from tests import test_oracle_routing as PR
 from tests import test_oracle_softmax as PS
+from tests import test_oracle_values as PV
 
 _orig = {n: getattr(O, n) for n in (
     "silu", "swiglu_group", "route_bwd", "sigmoid", "capacity", "unpermute", "unpermute_bwd",
@@ -150,6 +151,16 @@ def _softmax_without_max(logits):
     return (q / s).astype(np.float32)
 
 
+def _round_bf16_truncating(v):
+    m, e = np.frexp(np.asarray(v, dtype=np.float64))
+    return np.ldexp(np.trunc(m * 256.0) / 256.0, e)
+
+
+def _round_bf16_ties_away(v):
+    m, e = np.frexp(np.asarray(v, dtype=np.float64))
+    return np.ldexp(np.sign(m) * np.floor(np.abs(m) * 256.0 + 0.5) / 256.0, e)
+
+
 def _pairwise_sum_sequential(q):
     q = np.asarray(q, dtype=np.float32)
     acc = np.zeros(q.shape[:-1], dtype=np.float32)
@@ -241,6 +252,17 @@ MUTANTS = {
         lambda: PL.test_backward_matches_finite_differences("no_renorm")),
     "softmax without the max subtraction": (
         {"softmax_f32": _softmax_without_max}, PS.test_softmax_bits_invariant_under_a_shift_of_the_logits),
+    "bf16 decode shifted by 15 bits": (
+        {"decode": lambda a: ((a.astype(np.uint32) << np.uint32(15)).view(np.float32).astype(np.float64)
+                              if a.dtype == np.uint16 else np.asarray(a, dtype=np.float64))},
+        PV.test_decode_bf16_bits_matches_torch),
+    "bf16 rounding truncates": (
+        {"round_bf16": _round_bf16_truncating}, PV.test_round_bf16_matches_torch_rne),
+    "bf16 rounding ties away from zero": (
+        {"round_bf16": _round_bf16_ties_away}, PV.test_round_bf16_matches_torch_rne),
+    "capacity from the double, not the fp32, capacity factor": (
+        {"capacity": lambda cf, S_j, K, E: int(math.ceil(float(cf) * S_j * K / E))},
+        PV.test_capacity_takes_the_fp32_capacity_factor),
     "softmax sum left to right": (
         {"pairwise_sum_f32": _pairwise_sum_sequential}, PS.test_pairwise_sum_order),
     "ETP shard: gate rows used for up": (
