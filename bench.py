@@ -38,7 +38,23 @@ import sys
 import tempfile
 import time
 
-import numpy as np
+
+def _reference_arm_rank0_under_torchrun() -> bool:
+    argv = sys.argv[1:]
+    ref = "--impl=reference" in argv or any(
+        a == "--impl" and i + 1 < len(argv) and argv[i + 1] == "reference" for i, a in enumerate(argv))
+    return (ref and os.environ.get("RANK", "0") == "0"
+            and int(os.environ.get("LOCAL_WORLD_SIZE", "1")) > 1)
+
+
+# The reference arm's CPU oracle runs on rank 0 alone (the other ranks exit),
+# so it may use every core of the process's affinity mask, although torchrun
+# sets OMP_NUM_THREADS=1 for each rank; BLAS reads these when numpy loads.
+if _reference_arm_rank0_under_torchrun():
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        os.environ[_v] = str(len(os.sched_getaffinity(0)))
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -50,6 +66,16 @@ METRIC = "MoE layer tokens/s on 1 GB300"
 
 # ---------------------------------------------------------------------------
 # multi-rank bookkeeping (host logic; also exercised by CPU tests with gloo)
+
+def host_threads() -> int:
+    """Threads the oracle's BLAS uses: the affinity mask, unless a thread
+    count variable (read by BLAS when numpy loads) lowers it."""
+    n = len(os.sched_getaffinity(0))
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return max(1, min(n, int(os.environ[v])))
+    return n
+
 
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -159,7 +185,7 @@ def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = Non
     if cfg.backward:
         total *= 3.0   # backward: two GEMMs per forward GEMM (dgrad + wgrad)
     wall = time.perf_counter() - t0
-    return {"value": cfg.T / total, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+    return {"value": cfg.T / total, "unit": "tokens/s", "cores": host_threads(),
             "kind": "oracle",
             "sample": (f"routing, map, permute and combine on {T} of {cfg.T} tokens; expert FFN "
                        f"on {len(rows)} rows of expert 0 plus one expert's weight decode, "
@@ -474,7 +500,7 @@ def main():
             bwd_tf = 12.0 * n_kept * cfg.d * cfg.F / (bwd_ms * 1e-3) / 1e12
             line["stages"].update(ffn_bwd_ms=bwd_ms, ffn_bwd_tflops=bwd_tf,
                                   ffn_bwd_frac=bwd_tf / bf16_peak)
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:   # rank 0 at N = 1 only
             line["cpu_baseline"] = oracle_throughput(cfg, inp)
         print(json.dumps(line), flush=True)
     if dist is not None:

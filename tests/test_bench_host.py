@@ -84,3 +84,32 @@ def test_route_bytes():
     q = get_config("qwen2_57b_a14b")
     assert bench.route_algorithmic_bytes(q) == (
         8192 * 3584 * 2 + 64 * 3584 * 2 + 8192 * 64 * 4 + 3584 * 2 + 8192 * 4 + 8192 * 8 * 13)
+
+
+def test_oracle_thread_count(monkeypatch):
+    import bench
+    n = len(os.sched_getaffinity(0))
+    monkeypatch.delenv("OPENBLAS_NUM_THREADS", raising=False)
+    monkeypatch.delenv("OMP_NUM_THREADS", raising=False)
+    assert bench.host_threads() == n
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")      # what torchrun sets per rank
+    assert bench.host_threads() == 1
+    monkeypatch.setenv("OPENBLAS_NUM_THREADS", str(n + 7))
+    assert bench.host_threads() == n
+
+
+def test_reference_arm_rank0_detection(monkeypatch):
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("LOCAL_WORLD_SIZE", "2")
+    for argv, want in ([["bench.py", "--impl", "reference"], True],
+                       [["bench.py", "--impl=reference", "--gpus", "2"], True],
+                       [["bench.py", "--gpus", "2"], False]):
+        monkeypatch.setattr("sys.argv", argv)
+        assert bench._reference_arm_rank0_under_torchrun() is want
+    monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference"])
+    monkeypatch.setenv("RANK", "1")
+    assert not bench._reference_arm_rank0_under_torchrun()
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("LOCAL_WORLD_SIZE", "1")
+    assert not bench._reference_arm_rank0_under_torchrun()
