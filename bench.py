@@ -148,13 +148,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 
-def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = None) -> dict:
+ORACLE_FFN_FLOP_BUDGET = 4e12   # fp64 work of the CPU baseline's FFN sample
+
+
+def oracle_throughput(cfg, inp, ffn_rows: int | None = None, token_cap: int | None = None) -> dict:
     """Time the oracle as it stands on a bounded sample and scale to tokens/s.
 
     Routing, map, permute and combine run on `token_cap` tokens (all T by
-    default); the expert FFN runs the oracle's per-expert group routine on
-    `ffn_rows` rows of expert 0 (weight decode + the rows' GEMMs), scaled to
-    every expert's decode and all kept rows."""
+    default). The expert FFN runs the oracle's per-expert group routine
+    (weight decode + the rows' GEMMs) on whole experts 0, 1, ... while their
+    work (6 d F FLOP per row) fits ORACLE_FFN_FLOP_BUDGET, at least on the
+    first ORACLE_FFN_FLOP_BUDGET's worth of expert 0's rows; `ffn_rows` caps
+    the rows per expert instead. The times are scaled to every expert's
+    decode and all kept rows."""
     from oracle import moe_oracle as O
     T = cfg.T if token_cap is None else min(cfg.T, token_cap)
     sub = dict(inp)
@@ -166,29 +172,39 @@ def oracle_throughput(cfg, inp, ffn_rows: int = 256, token_cap: int | None = Non
     counts, offsets, row_of, src_of, n_kept = O.build_map(r["topk_idx"], r["keep"], c.E)
     Xp = O.permute(sub["x"], src_of, c.K)
     t_route = time.perf_counter() - t0
-    rows = np.arange(min(ffn_rows, max(1, int(counts[0]))))
-    t1 = time.perf_counter()
-    Wgu = O.decode(inp["W_gu"][0])
-    Wd = O.decode(inp["W_down"][0])
-    t_decode = time.perf_counter() - t1
-    t2 = time.perf_counter()
-    O.swiglu_group(O.decode(Xp[rows + offsets[0]]), Wgu, Wd, O.act_rounder(cfg.dtype, True))
-    t_rows = time.perf_counter() - t2
+    row_flop = 6.0 * cfg.d * cfg.F
+    cap = ffn_rows if ffn_rows is not None else max(64, int(ORACLE_FFN_FLOP_BUDGET / row_flop))
+    t_decode, t_rows, n_rows, experts = 0.0, 0.0, 0, 0
+    for e in range(c.E):
+        rows = np.arange(min(cap, int(counts[e])))
+        if rows.size == 0:
+            continue
+        if experts and (ffn_rows is not None or (n_rows + rows.size) * row_flop > ORACLE_FFN_FLOP_BUDGET):
+            break
+        t1 = time.perf_counter()
+        Wgu = O.decode(inp["W_gu"][e])
+        Wd = O.decode(inp["W_down"][e])
+        t2 = time.perf_counter()
+        O.swiglu_group(O.decode(Xp[rows + offsets[e]]), Wgu, Wd, O.act_rounder(cfg.dtype, True))
+        t_rows += time.perf_counter() - t2
+        t_decode += t2 - t1
+        n_rows += rows.size
+        experts += 1
     Yp = np.zeros((n_kept, c.d))
     t3 = time.perf_counter()
     O.unpermute(Yp, row_of, r["topk_w"], dtype=c.dtype)
     t_comb = time.perf_counter() - t3
     n_full = n_kept * cfg.T / T
-    total = (t_route + t_comb) * cfg.T / T + cfg.E * t_decode + t_rows * n_full / len(rows)
+    total = (t_route + t_comb) * cfg.T / T + cfg.E * t_decode / experts + t_rows * n_full / n_rows
     if cfg.Fs:
-        total += t_rows * cfg.T / len(rows) * cfg.Fs / cfg.F
+        total += t_rows * cfg.T / n_rows * cfg.Fs / cfg.F
     if cfg.backward:
         total *= 3.0   # backward: two GEMMs per forward GEMM (dgrad + wgrad)
     wall = time.perf_counter() - t0
     return {"value": cfg.T / total, "unit": "tokens/s", "cores": host_threads(),
             "kind": "oracle",
             "sample": (f"routing, map, permute and combine on {T} of {cfg.T} tokens; expert FFN "
-                       f"on {len(rows)} rows of expert 0 plus one expert's weight decode, "
+                       f"on {n_rows} rows of {experts} expert(s) with their weight decode, "
                        f"scaled to {cfg.E} experts and {int(n_full)} kept rows"
                        + ("; backward counted as 2x the forward GEMMs" if cfg.backward else "")),
             "sample_seconds": round(wall, 2)}

@@ -113,3 +113,16 @@ def test_reference_arm_rank0_detection(monkeypatch):
     monkeypatch.setenv("RANK", "0")
     monkeypatch.setenv("LOCAL_WORLD_SIZE", "1")
     assert not bench._reference_arm_rank0_under_torchrun()
+
+
+def test_oracle_baseline_sample_is_bounded():
+    import bench
+    from synthetic import get_config, make_inputs
+    cfg = get_config("mixtral_8x22b@small")
+    r = bench.oracle_throughput(cfg, make_inputs(cfg))
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] >= 1
+    assert "expert(s) with their weight decode" in r["sample"]
+    # the FFN sample is sized by its fp64 work: one Llama3-8x70B row is 1.4 GFLOP,
+    # so its sample stops well short of the 8192 rows of one expert
+    big = get_config("llama3_8x70b")
+    assert int(bench.ORACLE_FFN_FLOP_BUDGET / (6.0 * big.d * big.F)) < 4096
