@@ -1,12 +1,24 @@
 // C ABI of libmoe.so: argument checks, workspace layout, kernel launches.
 // The operations and their sources are documented in include/moe.h.
+// Every call that launches work opens an NVTX range named after itself, so
+// profilers that record NVTX show where each layer step starts and ends
+// (without a profiler attached the range calls return at once).
 #include <cstring>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "common.cuh"
 
 using namespace moe;
 
 namespace {
+
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
@@ -115,6 +127,7 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
                        const void *w_sg, float *logits, float *gate_logit, int32_t *topk_idx,
                        float *topk_prob, float *topk_w, uint8_t *keep, void *ws,
                        moe_stream_t stream) {
+  NvtxRange trace("moe_route");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!x || !W_r || !logits || !topk_idx || !topk_prob || !topk_w || !keep || !ws)
     return MOE_ERR_INVALID_ARG;
@@ -142,6 +155,7 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
 moe_status_t moe_route_topk(const moe_shape_t *shape, const float *logits, int32_t *topk_idx,
                             float *topk_prob, float *topk_w, uint8_t *keep, void *ws,
                             moe_stream_t stream) {
+  NvtxRange trace("moe_route_topk");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!logits || !topk_idx || !topk_prob || !topk_w || !keep || !ws || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
@@ -157,6 +171,7 @@ moe_status_t moe_route_topk(const moe_shape_t *shape, const float *logits, int32
 moe_status_t moe_permute(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
                          const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
                          int32_t *counts, int32_t *offsets, void *ws, moe_stream_t stream) {
+  NvtxRange trace("moe_permute");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets || !ws)
     return MOE_ERR_INVALID_ARG;
@@ -180,6 +195,7 @@ int64_t moe_padded_capacity(const moe_shape_t *shape) {
 moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
                                 const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
                                 int32_t *counts, int32_t *offsets, void *ws, moe_stream_t stream) {
+  NvtxRange trace("moe_permute_padded");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!shape->drop) return MOE_ERR_UNSUPPORTED;   // dropless routing has no fixed capacity
   if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets || !ws)
@@ -201,6 +217,7 @@ moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x, const i
 moe_status_t moe_permute_noalloc(const moe_shape_t *shape, const void *x, const int32_t *topk_idx,
                                  const uint8_t *keep, void *Xp, int32_t *row_of, int32_t *src_of,
                                  int32_t *counts, int32_t *offsets, moe_stream_t stream) {
+  NvtxRange trace("moe_permute_noalloc");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets)
     return MOE_ERR_INVALID_ARG;
@@ -228,6 +245,7 @@ moe_status_t moe_expert_ffn(int32_t dtype, int64_t max_rows, int32_t d, int32_t 
                             int32_t n_groups, const int32_t *offsets, const void *Xp,
                             const void *W_gu, const void *W_down, void *A_save, void *H_save,
                             void *Yp, void *ws, moe_stream_t stream) {
+  NvtxRange trace("moe_expert_ffn");
   moe_status_t st = ffn_check(dtype, max_rows, d, F, n_groups, offsets, ws);
   if (st != MOE_OK) return st;
   if (!Xp || !W_gu || !W_down || !H_save || !Yp) return MOE_ERR_INVALID_ARG;
@@ -245,6 +263,7 @@ moe_status_t moe_expert_ffn(int32_t dtype, int64_t max_rows, int32_t d, int32_t 
 moe_status_t moe_unpermute(const moe_shape_t *shape, const void *Yp, const int32_t *row_of,
                            const float *topk_w, const void *Ys, const float *gate_logit, void *out,
                            moe_stream_t stream) {
+  NvtxRange trace("moe_unpermute");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!Yp || !row_of || !topk_w || !out) return MOE_ERR_INVALID_ARG;
   if ((Ys == nullptr) != (gate_logit == nullptr)) return MOE_ERR_INVALID_ARG;
@@ -259,6 +278,7 @@ moe_status_t moe_unpermute_bwd(const moe_shape_t *shape, const void *dout, const
                                const int32_t *row_of, const float *topk_w, const void *Ys,
                                const float *gate_logit, void *dYp, float *dw, void *dYs, float *dz,
                                moe_stream_t stream) {
+  NvtxRange trace("moe_unpermute_bwd");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!dout || !Yp || !row_of || !topk_w || !dYp || !dw) return MOE_ERR_INVALID_ARG;
   const bool sh = Ys != nullptr;
@@ -279,6 +299,7 @@ moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int3
                                 const void *W_gu, const void *W_down, void *dA, float *dXp,
                                 float *dW_gu, float *dW_down, void *ws, size_t ws_bytes,
                                 moe_stream_t stream) {
+  NvtxRange trace("moe_expert_ffn_bwd");
   moe_status_t st = ffn_check(dtype, max_rows, d, F, n_groups, offsets, ws);
   if (st != MOE_OK) return st;
   if (ws_bytes < MOE_FFN_BWD_WORKSPACE_BYTES) return MOE_ERR_INVALID_ARG;
@@ -303,6 +324,7 @@ moe_status_t moe_expert_ffn_bwd(int32_t dtype, int64_t max_rows, int32_t d, int3
 
 moe_status_t moe_permute_bwd(const moe_shape_t *shape, const float *dXp, const int32_t *row_of,
                              const float *dx_add, float *dx, moe_stream_t stream) {
+  NvtxRange trace("moe_permute_bwd");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!dXp || !row_of || !dx || !aligned16(dXp) || !aligned16(dx) || (dx_add && !aligned16(dx_add)))
     return MOE_ERR_INVALID_ARG;
@@ -312,6 +334,7 @@ moe_status_t moe_permute_bwd(const moe_shape_t *shape, const float *dXp, const i
 
 moe_status_t moe_sum_partials(int32_t dtype, int32_t n_parts, int64_t rows, int32_t d,
                               const void *partials, void *out, moe_stream_t stream) {
+  NvtxRange trace("moe_sum_partials");
   if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_INVALID_ARG;
   if (n_parts < 1 || n_parts > 16 || rows < 0 || d < 1) return MOE_ERR_INVALID_ARG;
   if (d % (dtype == MOE_BF16 ? 8 : 4) != 0) return MOE_ERR_INVALID_ARG;
@@ -330,6 +353,7 @@ moe_status_t moe_route_bwd(const moe_shape_t *shape, const void *x, const void *
                            const float *topk_prob, const float *topk_w, const float *dw,
                            const float *dz, const float *dx_in, float *dW_r, float *db_r,
                            float *dw_sg, float *dx_router, void *ws, moe_stream_t stream) {
+  NvtxRange trace("moe_route_bwd");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!x || !W_r || !logits || !topk_idx || !topk_prob || !topk_w || !dw || !dW_r || !dx_router || !ws)
     return MOE_ERR_INVALID_ARG;
