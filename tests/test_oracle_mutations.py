@@ -161,6 +161,43 @@ def _round_bf16_ties_away(v):
     return np.ldexp(np.sign(m) * np.floor(np.abs(m) * 256.0 + 0.5) / 256.0, e)
 
 
+def _route_bwd_db_from_dp(x, W_r, p, idx, prob, w, dw, renorm, w_sg=None, dz=None, mirror=True):
+    """db_r summed from dp (before the softmax Jacobian) instead of dl."""
+    r = _orig["route_bwd"](x, W_r, p, idx, prob, w, dw, renorm, w_sg, dz, mirror=mirror)
+    dp = np.zeros_like(np.asarray(p, dtype=np.float64))
+    np.put_along_axis(dp, idx.astype(np.int64), np.asarray(dw, dtype=np.float64), axis=1)
+    r["db_r"] = O.f32_rounder(mirror)(dp.sum(axis=0))
+    return r
+
+
+def _unpermute_bwd_dz_without_sigmoid_slope(dout, Yp, row_of, w, Ys=None, z=None, *a, **k):
+    r = _orig["unpermute_bwd"](dout, Yp, row_of, w, Ys, z, *a, **k)
+    if Ys is not None:
+        s = _orig["sigmoid"](z)
+        r["dz"] = r["dz"] / (s * (1.0 - s))
+    return r
+
+
+def _build_map_padded_tokens_descending(idx, keep, E, C):
+    T, K = idx.shape
+    counts = np.zeros(E, dtype=np.int32)
+    row_of = np.full((T, K), -1, dtype=np.int32)
+    src_of = np.full(E * C, -1, dtype=np.int32)
+    for t in range(T - 1, -1, -1):
+        for k in range(K):
+            if keep[t, k]:
+                e = int(idx[t, k])
+                row = e * C + int(counts[e])
+                row_of[t, k] = row
+                src_of[row] = t * K + k
+                counts[e] += 1
+    return counts, (np.arange(E + 1) * C).astype(np.int32), row_of, src_of
+
+
+def _permute_padded_without_zero_fill(x, src_of, K):
+    return x[np.maximum(src_of, 0) // K]
+
+
 def _pairwise_sum_sequential(q):
     q = np.asarray(q, dtype=np.float32)
     acc = np.zeros(q.shape[:-1], dtype=np.float32)
@@ -263,6 +300,18 @@ MUTANTS = {
     "capacity from the double, not the fp32, capacity factor": (
         {"capacity": lambda cf, S_j, K, E: int(math.ceil(float(cf) * S_j * K / E))},
         PV.test_capacity_takes_the_fp32_capacity_factor),
+    "router backward: db_r summed before the softmax Jacobian": (
+        {"route_bwd": _route_bwd_db_from_dp},
+        lambda: PL.test_backward_matches_finite_differences("dropless_shared_bias")),
+    "shared gate backward: dz without the sigmoid slope": (
+        {"unpermute_bwd": _unpermute_bwd_dz_without_sigmoid_slope},
+        lambda: PL.test_backward_matches_finite_differences("dropless_shared_bias")),
+    "padded map: tokens descending inside an expert": (
+        {"build_map_padded": _build_map_padded_tokens_descending},
+        PR.test_padded_map_is_the_compact_map_with_fixed_strides),
+    "padded permute: padding rows not zeroed": (
+        {"permute_padded": _permute_padded_without_zero_fill},
+        PR.test_padded_map_is_the_compact_map_with_fixed_strides),
     "softmax sum left to right": (
         {"pairwise_sum_f32": _pairwise_sum_sequential}, PS.test_pairwise_sum_order),
     "ETP shard: gate rows used for up": (
