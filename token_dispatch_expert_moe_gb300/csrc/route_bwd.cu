@@ -12,6 +12,11 @@
 //   3. wgrad_partial_kernel: per chunk of tokens, partial sums of dl^T x (and
 //      dz^T x), register-tiled; reduce_kernel adds the chunks in order:
 //      deterministic, no atomics.
+// bf16 layers with d % 256 == 0 take steps 2 and 3 to the tensor cores
+// instead (the section "Tensor-core path" below): dl is split into three
+// bf16 planes, dx_router and dW_r become grouped-GEMM calls (gemm_tc.cu),
+// and plane_sum_kernel adds the planes and token chunks in order; with a
+// dx_in addend (a shared expert) dx stays on dx_kernel.
 #include "common.cuh"
 #include "softmax.cuh"
 
