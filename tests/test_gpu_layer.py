@@ -44,17 +44,18 @@ def test_layer_forward_backward(name):
             assert_close(k, host(g[k]), gr[k], cfg.dtype)
 
 
-@pytest.mark.parametrize("name", ["qwen2_57b_a14b@small", "mixtral_8x22b_g8t8@small"])
+@pytest.mark.parametrize("name", SMALL)
 def test_layer_deterministic(name):
     lib()
     cfg = get_config(name)
     inp = make_inputs(cfg, need_backward=True)
-    layer = _layer(cfg, inp, True)
+    bwd = cfg.backward or cfg.dtype == "bf16"
+    layer = _layer(cfg, inp, bwd)
     x, dout = dev(inp["x"]), dev(inp["dout"])
     runs = []
     for _ in range(2):
         out = layer.forward(x).clone()
-        g = {k: v.clone() for k, v in layer.backward(dout).items()}
+        g = {k: v.clone() for k, v in layer.backward(dout).items()} if bwd else {}
         runs.append((out, g))
     assert torch.equal(runs[0][0], runs[1][0])
     for k in runs[0][1]:
