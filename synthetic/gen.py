@@ -19,7 +19,9 @@ CHUNK = 1 << 22
 
 # Tensor ids: one per named input, fixed for all workloads.
 TID = {"x": 1, "W_r": 2, "b_r": 3, "w_sg": 4, "W_gu": 5, "W_down": 6,
-       "Ws_gu": 7, "Ws_down": 8, "dout": 9, "logits": 10}
+       "Ws_gu": 7, "Ws_down": 8, "dout": 9, "logits": 10,
+       # stand-alone inputs of single calls (the stage tests at full size)
+       "Yp": 11, "Ys": 12, "gate_logit": 13, "dXp": 14, "dx_add": 15}
 
 _THREADS = max(1, min(32, len(os.sched_getaffinity(0))))
 

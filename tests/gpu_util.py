@@ -1,18 +1,28 @@
 """Helpers of the GPU parity tests: device transfer, tolerances, configs.
 
-Tolerances: bf16 layers, relative Frobenius error <= 5e-3 and max-abs <= 3e-2
-on outputs and gradients, the max-abs bound scaled by max(1, RMS of the
-reference): gradients that sum over thousands of tokens (dW_r, dW_gu, dW_down
-reach 1e2..1e3) carry the bf16 rounding noise of the activations they are
-built from in proportion to their size, so a fixed 3e-2 only has meaning at
-unit scale, where the scaled and the fixed bounds coincide; fp32 layers, relative Frobenius <= 1e-5 and max-abs
-<= 1e-5 * max(1, max|ref|) (fp32 accumulation over the reduction depths used
-here keeps the error a few ulp of the largest value); router logits,
-relative Frobenius <= 1e-5; every index, mask, map and count bit-exact.
-Stored bf16 intermediates (A = [G|U], H, Yp, dA) are checked with the same
-relative Frobenius bound and a per-element bound of max(3e-2, one bf16 ulp of
-the reference): an fp32 accumulator and an fp64 value that straddle a bf16
-rounding boundary round one ulp apart, and above |v| = 4 one ulp exceeds 3e-2.
+Tolerances (bf16 layers: relative Frobenius error <= 5e-3 and max-abs
+<= 3e-2; fp32 layers: 1e-5), applied by the kind of tensor:
+  "output"  fp32 results (dx, dXp, dx_router, dw, dz) of bf16 layers:
+            rel-Frobenius <= 5e-3 and max-abs <= 3e-2, as stated;
+  "act"     values stored in bf16 (out, Yp, H, A_save, dA, dYp, dYs):
+            rel-Frobenius <= 5e-3 and, per element, |err| <= max(3e-2, one
+            bf16 ulp of the reference): an fp32 accumulator and the fp64
+            value that straddle a bf16 rounding boundary round one ulp
+            apart, and above |v| = 4 one bf16 ulp exceeds 3e-2, so no bf16
+            storage can meet the literal bound there; below 4 the bound is
+            the literal 3e-2;
+  "wgrad"   token-summed gradients (dW_*, dWs_*, db_r, dw_sg):
+            rel-Frobenius <= 5e-3 and max-abs <= 3e-2 x max(1, RMS of the
+            reference): they sum the bf16 rounding noise of the activations
+            over thousands of tokens and reach 1e2..1e3, so a fixed 3e-2 has
+            meaning only at unit scale, where the two bounds coincide;
+fp32 layers: rel-Frobenius <= 1e-5 and max-abs <= 1e-5 x max(1, max|ref|)
+(fp32 accumulation over the reduction depths used here keeps the error a few
+ulp of the largest value). Router logits: rel-Frobenius <= 1e-5. Every
+index, mask, map and count bit-exact.
+
+Every comparison records its measured rel-Frobenius and max-abs beside the
+literal bound (3e-2); the session prints the tightest margins at the end.
 """
 from __future__ import annotations
 
@@ -82,20 +92,51 @@ def bf16_ulp(v):
     return 2.0 ** (e - 7)
 
 
-def assert_close(name, got, ref, dtype, kind="output"):
+# measured errors of every passing comparison of this session (printed at its end)
+MARGINS = []
+
+_WGRAD = ("dW", "dWs", "db_r", "dw_sg")
+_ACT = ("out", "Yp", "H", "A_save", "dA", "dYp", "dYs")
+
+
+def kind_of(name: str) -> str:
+    base = name.split("[")[0].split(" ")[0]
+    if base.startswith(_WGRAD):
+        return "wgrad"
+    if base in _ACT:
+        return "act"
+    return "output"
+
+
+def assert_close(name, got, ref, dtype, kind=None):
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    kind = kind or kind_of(name)
     rf = rel_frob(got, ref)
-    ma = float(np.abs(got - ref).max()) if got.size else 0.0
+    err = np.abs(got - ref)
+    ma = float(err.max()) if got.size else 0.0
     mref = float(np.abs(ref).max()) if ref.size else 0.0
+    over_literal = int(np.count_nonzero(err > 3e-2))
     if dtype == "bf16" and kind == "act":
-        ok = rf <= 5e-3 and bool(np.all(np.abs(got - ref) <= np.maximum(3e-2, bf16_ulp(ref))))
-    elif dtype == "bf16":
+        bound = np.maximum(3e-2, bf16_ulp(ref))
+        ok = rf <= 5e-3 and bool(np.all(err <= bound))
+        ma_bound = float(bound.max()) if ref.size else 3e-2
+    elif dtype == "bf16" and kind == "wgrad":
         rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
-        ok = rf <= 5e-3 and ma <= 3e-2 * max(1.0, rms)
+        ma_bound = 3e-2 * max(1.0, rms)
+        ok = rf <= 5e-3 and ma <= ma_bound
+    elif dtype == "bf16":
+        ma_bound = 3e-2
+        ok = rf <= 5e-3 and ma <= ma_bound
     else:
-        ok = rf <= 1e-5 and ma <= 1e-5 * max(1.0, mref)
-    assert ok, f"{name}: rel_frob {rf:.3e} max_abs {ma:.3e} (max|ref| {mref:.3g}, {dtype})"
+        ma_bound = 1e-5 * max(1.0, mref)
+        ok = rf <= 1e-5 and ma <= ma_bound
+    if ok:   # comparisons that pass (a failing one is reported by its assertion)
+        MARGINS.append({"name": name, "dtype": dtype, "kind": kind, "rel_frob": rf, "max_abs": ma,
+                        "max_ref": mref, "max_abs_bound": ma_bound,
+                        "n_over_3e-2": over_literal, "n": int(got.size)})
+    assert ok, (f"{name} ({kind}): rel_frob {rf:.3e} max_abs {ma:.3e} (bound {ma_bound:.3e}, "
+                f"max|ref| {mref:.3g}, {over_literal} of {got.size} above 3e-2, {dtype})")
     return rf, ma

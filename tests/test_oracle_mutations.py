@@ -11,13 +11,15 @@ import pytest
 
 from oracle import moe_oracle as O
 from tests import test_oracle_layer as PL
+from tests import test_oracle_rounding_points as PRP
 from tests import test_oracle_routing as PR
 from tests import test_oracle_softmax as PS
 from tests import test_oracle_values as PV
 
 _orig = {n: getattr(O, n) for n in (
     "silu", "swiglu_group", "route_bwd", "sigmoid", "capacity", "unpermute", "unpermute_bwd",
-    "permute_bwd", "sum_partials", "router_logits", "padded_capacity", "route", "expert_ffn")}
+    "permute_bwd", "sum_partials", "router_logits", "padded_capacity", "route", "expert_ffn",
+    "swiglu_group_bwd")}
 
 
 # ---- mutants ----
@@ -218,6 +220,54 @@ def _padded_capacity_unclipped(T, S, K, E, cf):
     return sum(O.capacity(cf, min(S, T - lo), K, E) for lo in range(0, T, S))
 
 
+def _swiglu_h_from_rounded_gu(X, Wgu, Wdown, rnd):
+    F = Wgu.shape[0] // 2
+    Acc = X @ Wgu.T
+    G, U = rnd(Acc[:, :F]), rnd(Acc[:, F:])
+    H = rnd(O.silu(G) * U)
+    return rnd(Acc), H, rnd(H @ Wdown.T)
+
+
+def _swiglu_y_from_unrounded_h(X, Wgu, Wdown, rnd):
+    F = Wgu.shape[0] // 2
+    Acc = X @ Wgu.T
+    h = O.silu(Acc[:, :F]) * Acc[:, F:]
+    return rnd(Acc), rnd(h), rnd(h @ Wdown.T)
+
+
+def _swiglu_bwd_rounding(round_dh=False, dx_from_unrounded=False):
+    def f(dY, X, A, H, Wgu, Wdown, rnd, r32):
+        F = Wgu.shape[0] // 2
+        dH = dY @ Wdown
+        if round_dh:
+            dH = rnd(dH)
+        G, U = A[:, :F], A[:, F:]
+        sg = 1.0 / (1.0 + np.exp(-G))
+        dA_raw = np.concatenate([dH * U * sg * (1.0 + G * (1.0 - sg)), dH * G * sg], axis=1)
+        dA = rnd(dA_raw)
+        dX = r32((dA_raw if dx_from_unrounded else dA) @ Wgu)
+        return dX, r32(dY.T @ H), r32(dA.T @ X), dA
+    return f
+
+
+def _unpermute_rounds_each_term(Yp, row_of, w, Ys=None, z=None, dtype="bf16", mirror=True,
+                                tokens=None):
+    rnd = O.act_rounder(dtype, mirror)
+    T, K = row_of.shape
+    acc = np.zeros((T, Yp.shape[1]))
+    for k in range(K):
+        r = row_of[:, k]
+        m = r >= 0
+        acc[m] += rnd(np.asarray(w, dtype=np.float64)[m, k][:, None] * Yp[r[m]])
+    return rnd(acc)
+
+
+def _unpermute_bwd_dyp_unrounded(dout, Yp, row_of, w, *a, **k):
+    r = _orig["unpermute_bwd"](dout, Yp, row_of, w, *a, **dict(k, mirror=False))
+    ref = _orig["unpermute_bwd"](dout, Yp, row_of, w, *a, **k)
+    return dict(ref, dYp=r["dYp"])
+
+
 # name: (attribute -> replacement, the pin that must fail)
 MUTANTS = {
     "silu dropped (H = G*U)": (
@@ -317,6 +367,24 @@ MUTANTS = {
     "ETP shard: gate rows used for up": (
         {"fsplit_weights": _fsplit_gate_rows_twice},
         lambda: PL.test_fsplit_is_the_unsplit_ffn_in_exact_arithmetic(2)),
+    "SwiGLU: H from the bf16-rounded G and U": (
+        {"swiglu_group": _swiglu_h_from_rounded_gu}, PRP.test_forward_rounding_points),
+    "SwiGLU: Yp from the unrounded H": (
+        {"swiglu_group": _swiglu_y_from_unrounded_h}, PRP.test_forward_rounding_points),
+    "SwiGLU backward: dH rounded to bf16 before dA": (
+        {"swiglu_group_bwd": _swiglu_bwd_rounding(round_dh=True)}, PRP.test_backward_rounding_points),
+    "SwiGLU backward: dXp from the unrounded dA": (
+        {"swiglu_group_bwd": _swiglu_bwd_rounding(dx_from_unrounded=True)},
+        PRP.test_backward_rounding_points),
+    "combine: every weighted term rounded": (
+        {"unpermute": _unpermute_rounds_each_term}, PRP.test_combine_rounds_once_after_the_sum),
+    "un-permute backward: dYp not rounded": (
+        {"unpermute_bwd": _unpermute_bwd_dyp_unrounded},
+        PRP.test_unpermute_bwd_rounds_dyp_to_bf16_and_keeps_dw_fp32),
+    "permute backward: dx rounded to bf16": (
+        {"permute_bwd": lambda dXp, row_of, dx_add=None, mirror=True:
+            O.round_bf16(_orig["permute_bwd"](dXp, row_of, dx_add, mirror))},
+        PRP.test_permute_bwd_sums_in_fp32),
     "ETP partials summed in reverse shard order": (
         {"sum_partials": lambda parts, mirror=True: _orig["sum_partials"](parts[::-1], mirror)},
         PL.test_sum_partials_adds_in_shard_order_in_fp32),

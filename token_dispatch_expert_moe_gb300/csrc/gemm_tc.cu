@@ -530,24 +530,30 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
         ok = __all_sync(0xffffffffu, wait_bounded(st, ebar, ephase, p.status, 5));
         ephase ^= 1;
         if (!ok) break;
-        float dh[64];
-        tmem_ld32(tbase + c * 64, *reinterpret_cast<float(*)[32]>(dh));
-        tmem_ld32(tbase + c * 64 + 32, *reinterpret_cast<float(*)[32]>(dh + 32));
         uint8_t *rg = bg + lane * 128, *ru = bu + lane * 128;
+        // 32 columns per pass, the loop over the two passes kept rolled: a
+        // short loop body keeps the epilogue's instruction footprint small
+        // next to the producer and MMA warps that share the instruction cache
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float dh[32];
+          tmem_ld32(tbase + c * 64 + hh * 32, dh);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk ch = columns 8ch..8ch+7
-          const int off = (ch ^ (lane & 7)) << 4;
-          float G[8], U[8], dG[8], dU[8];
-          load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(rg + off), G);
-          load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
+          for (int cc = 0; cc < 4; ++cc) {   // 16-byte chunk ch = columns 8ch..8ch+7
+            const int off = ((hh * 4 + cc) ^ (lane & 7)) << 4;
+            float G[8], U[8], dG[8], dU[8];
+            load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(rg + off), G);
+            load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float sgm = 1.0f / (1.0f + __expf(-G[j]));
-            dG[j] = dh[8 * ch + j] * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
-            dU[j] = dh[8 * ch + j] * G[j] * sgm;
+            for (int j = 0; j < 8; ++j) {
+              const float sgm = __frcp_rn(1.0f + __expf(-G[j]));
+              const float dhv = dh[8 * cc + j];
+              dG[j] = dhv * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
+              dU[j] = dhv * G[j] * sgm;
+            }
+            store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(rg + off), dG);
+            store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(ru + off), dU);
           }
-          store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(rg + off), dG);
-          store16<__nv_bfloat16>(reinterpret_cast<__nv_bfloat16 *>(ru + off), dU);
         }
         fence_proxy_async();
         __syncwarp();
@@ -621,7 +627,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
             load16<__nv_bfloat16>(As + p.F + c * 32 + i, U);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float sg = 1.0f / (1.0f + __expf(-G[j]));
+              const float sg = __frcp_rn(1.0f + __expf(-G[j]));
               dG[j] = dh[i + j] * U[j] * sg * (1.0f + G[j] * (1.0f - sg));
               dU[j] = dh[i + j] * G[j] * sg;
             }

@@ -170,29 +170,43 @@ class MoELayer:
                                  self.dW_down[s], self.ws, stream)
         L.moe_sum_partials(L.MOE_F32, self.etp, self.rows, c.d, self.dX_parts, self.dXp, stream)
 
-    def backward(self, dout: torch.Tensor, stream=None, ffn_events=None) -> dict:
-        """ffn_events: optional (start, end) CUDA events recorded on the current
-        stream around the routed experts' moe_expert_ffn_bwd call."""
+    def backward(self, dout: torch.Tensor, stream=None, marks=None) -> dict:
+        """marks: optional dict of (start, end) CUDA event pairs, keyed by
+        "unpermute_bwd", "ffn_bwd" (routed experts), "shared_ffn_bwd",
+        "route_bwd" and "permute_bwd"; each present pair is recorded on the
+        current stream around that call."""
         c, s, w = self.cfg, self.shape, self.w
+        marks = marks or {}
+
+        def mark(name, i):
+            if name in marks:
+                marks[name][i].record()
+
+        mark("unpermute_bwd", 0)
         L.moe_unpermute_bwd(s, dout, self.Yp, self.row_of, self.topk_w, self.Ys, self.gate_logit,
                             self.dYp, self.dw, self.dYs if self.shared else None,
                             self.dz if self.shared else None, stream)
-        if ffn_events is not None:
-            ffn_events[0].record()
+        mark("unpermute_bwd", 1)
+        mark("ffn_bwd", 0)
         self.routed_ffn_bwd(stream)
-        if ffn_events is not None:
-            ffn_events[1].record()
+        mark("ffn_bwd", 1)
         dx_in = None
         if self.shared:
+            mark("shared_ffn_bwd", 0)
             L.moe_expert_ffn_bwd(self.dtype_code, c.T, c.d, c.Fs, 1, self.off1, self.dYs, self.x,
                                  self.As, self.Hs, w["Ws_gu"], w["Ws_down"], self.dAs, self.dXs,
                                  self.dWs_gu, self.dWs_down, self.ws, stream)
+            mark("shared_ffn_bwd", 1)
             dx_in = self.dXs
+        mark("route_bwd", 0)
         L.moe_route_bwd(s, self.x, w["W_r"], w.get("w_sg"), self.logits, self.topk_idx,
                         self.topk_prob, self.topk_w, self.dw, self.dz if self.shared else None,
                         dx_in, self.dW_r, self.db_r if "b_r" in w else None,
                         self.dw_sg if self.shared else None, self.dx_router, self.ws, stream)
+        mark("route_bwd", 1)
+        mark("permute_bwd", 0)
         L.moe_permute_bwd(s, self.dXp, self.row_of, self.dx_router, self.dx, stream)
+        mark("permute_bwd", 1)
         g = {"dx": self.dx, "dW_r": self.dW_r, "dW_gu": self.dW_gu, "dW_down": self.dW_down}
         if "b_r" in w:
             g["db_r"] = self.db_r
