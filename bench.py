@@ -367,6 +367,9 @@ def main():
     ap.add_argument("--etp", type=int, default=1,
                     help="run the routed experts F-split into this many shards (the arithmetic "
                          "of an expert-tensor-parallel group, on one GPU)")
+    ap.add_argument("--gather", action="store_true",
+                    help="forward-only bf16 workloads: fuse the permutation into the gate/up "
+                         "GEMM (map-only moe_permute + moe_expert_ffn_gather)")
     ap.add_argument("--override", default="",
                     help="profiling cases only: comma-separated field=value changes to the "
                          "workload, e.g. T=4096,E=16 (the JSON line then names the changed shape)")
@@ -399,7 +402,7 @@ def main():
     cfg_r = dataclasses.replace(cfg, seed=cfg.seed + rank)   # each replica its own batch
     inp = make_inputs(cfg_r)
     w = {k: to_device(v) for k, v in inp.items() if k not in ("x", "dout")}
-    layer = MoELayer(cfg_r, w, etp=args.etp, layout=args.layout)
+    layer = MoELayer(cfg_r, w, etp=args.etp, layout=args.layout, gather=args.gather)
     x = to_device(inp["x"])
     layer.x = x   # the backward reads the forward's tokens
     dout = to_device(inp["dout"]) if cfg.backward else None
@@ -499,6 +502,8 @@ def main():
     gemm_ms = ffn_ms + ffn_bwd_ms
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
     sb = stage_bytes(cfg, n_kept)
+    if args.gather:   # the permute call builds the map only; the GEMM reads x
+        sb["permute"] = cfg.T * cfg.K * 9 + n_kept * 4
     route_bytes = route_algorithmic_bytes(cfg)
     traffic = None
     tr_key = f"{cfg.name}:grouped_gemm" + (":fwd_bwd" if cfg.backward else "")
@@ -614,12 +619,14 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic (seeded normal inputs, random-init weights)",
             "config": dict(workload_config(cfg), **({"etp_shards": args.etp} if args.etp > 1 else {}),
-                           **({"layout": "padded"} if args.layout == "padded" else {})),
+                           **({"layout": "padded"} if args.layout == "padded" else {}),
+                           **({"permute": "fused into the gate/up GEMM"} if args.gather else {})),
             "clocks": clk,
             "e2e": {"value": e2e["value"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": (launches_per_step(cfg, args.etp)
-                             + (1 if args.layout == "padded" else 0)) * args.steps,
+                             + (1 if args.layout == "padded" else 0)
+                             - (1 if args.gather else 0)) * args.steps,
             "roofline": {"kernel": ("routed experts' grouped GEMMs, forward + backward (moe_expert_ffn: "
                                     "gate/up + down; moe_expert_ffn_bwd: dH, dXp, dW_down, dW_gu)"
                                     if cfg.backward else

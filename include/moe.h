@@ -69,7 +69,9 @@ typedef struct {
   int32_t drop;            /* 0 dropless, 1 capacity-factor dropping         */
   float capacity_factor;   /* CF, > 0 (used when drop = 1)                   */
   int64_t subseq_len;      /* S: drops are decided per block of S tokens of
-                              the flat order; 0 means S = T (full sequence)  */
+                              the flat order; 0 means S = T (full sequence);
+                              with drop = 1 the router needs S < 2^29
+                              (else MOE_ERR_UNSUPPORTED)                     */
   int32_t renorm;          /* 1: combine weights renormalised over the K     */
   int32_t Fs;              /* shared expert SwiGLU size, 0 = none            */
 } moe_shape_t;
@@ -137,7 +139,9 @@ moe_status_t moe_route_topk(const moe_shape_t *shape, const float *logits,
  *        row_of [T,K] int32: permuted row of each assignment, -1 if dropped;
  *        src_of [T*K] int32: t*K+k of each permuted row (first n_kept valid);
  *        Xp [T*K, d] dtype: Xp[row_of[t,k]] = x[t]; rows are expert-major and
- *        token-ascending inside an expert; rows >= n_kept are not written.  */
+ *        token-ascending inside an expert; rows >= n_kept are not written.
+ *        Xp may be NULL: then only the map is built and no row is copied
+ *        (for moe_expert_ffn_gather, which reads the rows from x itself). */
 moe_status_t moe_permute(const moe_shape_t *shape, const void *x,
                          const int32_t *topk_idx, const uint8_t *keep, void *Xp,
                          int32_t *row_of, int32_t *src_of, int32_t *counts,
@@ -181,16 +185,20 @@ moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x,
  * cudaMalloc/cudaFree can cause.
  * How: the map build's scratch (per-block expert counts, 128 KB) is a fixed
  * array inside libmoe.so, resident on every GPU that loads the library until
- * the process exits. The first call on each device looks the array's device
- * address up (cudaGetSymbolAddress, with that device current) and caches it;
- * make that first call before any stream capture. No call allocates.
+ * the process exits. The first call in each CUDA context (on each device, or
+ * again after cudaDeviceReset) looks the array's device address up
+ * (cudaGetSymbolAddress, with that device current) and caches it under the
+ * context's ID; make that first call before any stream capture. No call
+ * allocates.
  * Limits: T <= MOE_PERMUTE_NOALLOC_MAX_TOKENS, else MOE_ERR_UNSUPPORTED; E <= 64
  * as everywhere. Every call uses the same array: two calls that can run at the
  * same time on one GPU (different streams or host threads without ordering
  * between them) race and corrupt each other's maps; order them. Each call
  * rewrites all the scratch it reads, so the previous call's contents never
  * leak into a result. There is no workspace, so no device status word is
- * recorded: an out-of-range expert index is skipped (its row_of is -1).     */
+ * recorded: an out-of-range expert index is skipped (its row_of is -1), and
+ * a row copy whose bounded wait gave up (which would mean a stalled copy
+ * engine) leaves its token's rows of Xp unwritten without any report.      */
 moe_status_t moe_permute_noalloc(const moe_shape_t *shape, const void *x,
                                  const int32_t *topk_idx, const uint8_t *keep, void *Xp,
                                  int32_t *row_of, int32_t *src_of, int32_t *counts,
@@ -214,6 +222,26 @@ moe_status_t moe_expert_ffn(int32_t dtype, int64_t max_rows, int32_t d, int32_t 
                             int32_t n_groups, const int32_t *offsets, const void *Xp,
                             const void *W_gu, const void *W_down, void *A_save,
                             void *H_save, void *Yp, void *ws, moe_stream_t stream);
+
+/* The grouped SwiGLU FFN of moe_expert_ffn with the permutation fused into
+ * its gate/up GEMM (study notes, "method overview": the permutation feeds the
+ * experts' FFN directly): instead of reading Xp, the GEMM gathers permuted
+ * row R from x as x[src_of[R] / K], so the permuted copy of the tokens is
+ * neither written nor read back. Outputs equal moe_expert_ffn's on
+ * Xp = permute(x) bit for bit.
+ *   x [T, d] bf16 (the layer's tokens); src_of [>= offsets[n_groups]] int32
+ *   as written by moe_permute / moe_permute_padded (t*K + k of each permuted
+ *   row; a negative entry, the padded layout's padding rows, gives a zero
+ *   row); T, K as in moe_shape_t. Other arguments as moe_expert_ffn
+ *   (bf16 only; d % 128 == 0, F % 128 == 0).
+ * Errors: as moe_expert_ffn; an src_of entry >= T*K records MOE_ERR_DEVICE
+ *   in the status word and gives a zero row; MOE_ERR_UNSUPPORTED when the
+ *   CTA-pair GEMM kernels are disabled.                                      */
+moe_status_t moe_expert_ffn_gather(int64_t max_rows, int32_t d, int32_t F, int32_t n_groups,
+                                   const int32_t *offsets, const void *x, int64_t T, int32_t K,
+                                   const int32_t *src_of, const void *W_gu, const void *W_down,
+                                   void *A_save, void *H_save, void *Yp, void *ws,
+                                   moe_stream_t stream);
 
 /* Un-permutation with the weighted Top-K combine (study notes, "method
  * overview": the un-permutation restores the original token order).

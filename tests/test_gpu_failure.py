@@ -1,10 +1,12 @@
 """Failure detection without a GPU fault: the grouped GEMM's pipeline waits
-are bounded. With MOE_FAULT_INJECT_STALL=1 the TMA producer issues no loads,
-so the MMA warp waits on a barrier that nothing will complete; after about
-two seconds the kernel records MOE_ERR_TIMEOUT in the status word, stops every
+are bounded. The test build of the library (libmoe_testhooks.so, the same
+kernels with a fault-injection hook compiled in) runs in a process of its
+own: with MOE_FAULT_INJECT_STALL=1 the TMA producer issues no loads, so the
+MMA warp waits on a barrier that nothing will complete; after about two
+seconds the kernel records MOE_ERR_TIMEOUT in the status word, stops every
 warp role, releases its tensor memory and returns. The test reads the status
 on the host and then checks that the same context still computes correct
-results."""
+results. The product library (libmoe.so) has no such hook."""
 import os
 import subprocess
 import sys
@@ -41,7 +43,14 @@ def _run(L, d, F, offsets, n, Xp, W_gu, W_down, ws):
     return H, Y
 
 
-def test_gemm_wait_timeout_is_reported_and_context_survives(monkeypatch):
+def _under_test_build():
+    return os.environ.get("MOE_LIBRARY", "").endswith("libmoe_testhooks.so")
+
+
+def test_timeout_case(monkeypatch):
+    """Runs only inside the test build's process (see the two tests below)."""
+    if not _under_test_build():
+        pytest.skip("needs the test build of the library (run by the tests below)")
     L = lib()
     d, F, offsets, n, Xp, W_gu, W_down = _case()
     ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
@@ -64,12 +73,21 @@ def test_gemm_wait_timeout_is_reported_and_context_survives(monkeypatch):
     assert_close("Yp", host(Y), Yr, "bf16", "act")
 
 
-def test_single_cta_kernel_timeout_too():
+def _in_test_build(extra_env):
     lib()
+    from token_dispatch_expert_moe_gb300 import build
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = ("import sys, pytest; sys.exit(pytest.main(['-q', '-p', 'no:cacheprovider', "
-            "'tests/test_gpu_failure.py::test_gemm_wait_timeout_is_reported_and_context_survives']))")
-    env = dict(os.environ, MOE_GEMM_PAIR="0")
+            "'tests/test_gpu_failure.py::test_timeout_case']))")
+    env = dict(os.environ, MOE_LIBRARY=build.TEST_LIB, **extra_env)
     r = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True,
                        text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert r.returncode == 0 and "1 passed" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
+
+
+def test_pair_kernel_timeout():
+    _in_test_build({})
+
+
+def test_single_cta_kernel_timeout():
+    _in_test_build({"MOE_GEMM_PAIR": "0"})

@@ -128,15 +128,17 @@ def test_ffn_backward_group_layouts(rows, dtype):
 @pytest.mark.parametrize("pair", ["0", "1"])
 def test_single_cta_and_pair_kernels_agree(pair):
     """The CTA-pair and single-CTA grouped GEMMs both match the oracle (each
-    run in its own process, since the kernel choice is read once)."""
+    run in its own process with the test build of the library, whose
+    MOE_GEMM_PAIR switch selects the kernels and is read once)."""
     import os
     import subprocess
     import sys
     lib()
+    from token_dispatch_expert_moe_gb300 import build
     code = ("import sys; sys.argv=['x']; import pytest; "
             "sys.exit(pytest.main(['-q', '-p', 'no:cacheprovider', '-k', "
             "'group_layouts and bf16', 'tests/test_gpu_ffn.py']))")
-    env = dict(os.environ, MOE_GEMM_PAIR=pair)
+    env = dict(os.environ, MOE_GEMM_PAIR=pair, MOE_LIBRARY=build.TEST_LIB)
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True,
                        text=True, timeout=900)

@@ -91,13 +91,31 @@ def test_route_fused(name):
 
 
 # bf16 shapes whose row tiles (T / 128) leave SMs idle, so the tensor-core
-# logits split their K loop: 4 splits of 8 K blocks (gate logit and bias
-# ride along), 3 splits over 3 ragged row tiles, 2 splits of 8 K blocks
+# logits split their K loop over a cluster of CTAs (the even CTA adds the
+# parts in order and routes): 4 parts of 8 K blocks with E = 8; 3 parts with
+# the gate logit and bias riding along (E = 64 + 1 columns: the even CTA's
+# exchange buffer holds two other parts); 3 parts over 3 ragged row tiles;
+# 2 parts of 8 K blocks
 SPLIT_K = {
+    "split4_e8": ("mixtral_8x22b", dict(T=1000, d=2048, F=128, S=250)),
     "split4_gate_bias": ("qwen2_57b_a14b", dict(T=1000, d=2048, F=128, Fs=128)),
     "split3_ragged": ("mixtral_8x22b", dict(T=300, d=1536, F=128, S=100)),
     "split2_e64": ("mixtral_8x22b_g8t8", dict(T=2000, d=1024, F=128, S=500)),
 }
+
+
+# shapes whose router GEMM routes in its epilogue (no K split, E <= 16):
+# E = 16 with K = 4, and E = 9 (padded to 16 experts) with the bias
+FUSED = {
+    "e16_k4": ("mixtral_8x22b", dict(T=1500, d=512, F=128, E=16, K=4, S=500)),
+    "e9_bias": ("qwen2_57b_a14b", dict(T=700, d=512, F=128, E=9, K=3, Fs=0)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FUSED))
+def test_route_fused_epilogue(case):
+    base, kw = FUSED[case]
+    _check_route(dataclasses.replace(get_config(base), name=f"{base}@{case}", **kw))
 
 
 @pytest.mark.parametrize("case", sorted(SPLIT_K))

@@ -12,7 +12,9 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libmoe.so")
+# MOE_LIBRARY selects another build of the library (the tests point it at
+# libmoe_testhooks.so, the build with the failure-injection hooks)
+LIB_PATH = os.environ.get("MOE_LIBRARY") or os.path.join(PKG, "libmoe.so")
 
 MOE_F32, MOE_BF16 = 0, 1
 MOE_FFN_BWD_WORKSPACE_BYTES = 33280   # include/moe.h
@@ -42,7 +44,7 @@ def shape_of(cfg) -> MoEShape:
 
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
+    raise ImportError(f"the library is not built ({LIB_PATH}); run "
                       "`python -m token_dispatch_expert_moe_gb300.build`")
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -57,6 +59,8 @@ _SIGS = {
     "moe_permute_noalloc": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute_padded": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_expert_ffn": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_expert_ffn_gather": [_I64, _I32, _I32, _I32, _P, _P, _I64, _I32, _P, _P, _P, _P, _P, _P,
+                              _P, _P],
     "moe_unpermute": [_S, _P, _P, _P, _P, _P, _P, _P],
     "moe_unpermute_bwd": [_S, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_expert_ffn_bwd": [_I32, _I64, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -163,6 +167,13 @@ def moe_expert_ffn(dtype, max_rows, d, F, n_groups, offsets, Xp, W_gu, W_down, A
                    Yp, ws, stream=None):
     _call("moe_expert_ffn", dtype, max_rows, d, F, n_groups, _ptr(offsets), _ptr(Xp), _ptr(W_gu),
           _ptr(W_down), _ptr(A_save), _ptr(H_save), _ptr(Yp), _ptr(ws), _stream(stream))
+
+
+def moe_expert_ffn_gather(max_rows, d, F, n_groups, offsets, x, T, K, src_of, W_gu, W_down,
+                          A_save, H_save, Yp, ws, stream=None):
+    _call("moe_expert_ffn_gather", max_rows, d, F, n_groups, _ptr(offsets), _ptr(x), T, K,
+          _ptr(src_of), _ptr(W_gu), _ptr(W_down), _ptr(A_save), _ptr(H_save), _ptr(Yp), _ptr(ws),
+          _stream(stream))
 
 
 def moe_unpermute(shape, Yp, row_of, topk_w, Ys, gate_logit, out, stream=None):

@@ -32,8 +32,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+def _compile(src: str, extra: list[str], obj_name: str) -> str:
+    obj = os.path.join(BUILD, obj_name)
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -43,18 +43,34 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    """Compile and link libmoe.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + ".tmp"
+# The test build: the same library with the test hooks of gemm_tc.cu compiled
+# in (MOE_FAULT_INJECT_STALL, MOE_GEMM_PAIR); only the failure-path and
+# kernel-comparison tests load it, in processes of their own.
+TEST_LIB = os.path.join(PKG, "libmoe_testhooks.so")
+HOOKED = "gemm_tc.cu"
+
+
+def _link(objs: list[str], out: str) -> None:
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-ldl"]   # -ldl: NVTX loads a profiler's hooks
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
+
+
+def build(verbose_ptxas: bool = False) -> str:
+    """Compile and link libmoe.so (and the test build); returns libmoe.so's path."""
+    os.makedirs(BUILD, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    jobs = [(s, extra, s.replace(".cu", ".o")) for s in SOURCES]
+    jobs.append((HOOKED, ["-DMOE_TEST_HOOKS"], HOOKED.replace(".cu", "_hooks.o")))
+    with ThreadPoolExecutor(len(jobs)) as ex:
+        objs = list(ex.map(lambda j: _compile(*j), jobs))
+    prod = objs[:len(SOURCES)]
+    _link(prod, LIB)
+    hooked = [o for s, o in zip(SOURCES, prod) if s != HOOKED] + [objs[-1]]
+    _link(hooked, TEST_LIB)
     return LIB
 
 

@@ -43,7 +43,7 @@ int64_t subseq(const moe_shape_t *s) {
 }
 
 struct Layout {
-  size_t status, map, cap, rbwd, rpart, total;
+  size_t status, map, cap, capn, rbwd, total;
 };
 
 // the tensor-core router's logits path (bf16, d % 64 == 0)
@@ -58,16 +58,16 @@ Layout layout(const moe_shape_t *s) {
   L.map = off;
   off += align256((size_t)((s->T + 255) / 256) * s->E * sizeof(int32_t));
   L.cap = off;
+  L.capn = off;
   if (s->drop) {
     const int64_t S = subseq(s);
     const int64_t n_sub = (s->T + S - 1) / S;
     off += align256((size_t)n_sub * s->E * S * sizeof(unsigned long long));
+    L.capn = off;
+    off += align256((size_t)n_sub * s->E * sizeof(uint32_t));
   }
   L.rbwd = off;
   off += align256(route_bwd_workspace_bytes(s->T, s->d, s->E));
-  L.rpart = off;   // the router GEMM's K-split partial sums (any split count)
-  if (router_on_tensor_cores(s))
-    off += align256((size_t)kRouterMaxSplit * s->T * (s->E + 1) * sizeof(float));
   L.total = off > MOE_FFN_BWD_WORKSPACE_BYTES ? off : MOE_FFN_BWD_WORKSPACE_BYTES;
   return L;
 }
@@ -83,7 +83,17 @@ RouteArgs route_args(const moe_shape_t *s, void *ws) {
   a.renorm = s->renorm; a.drop = s->drop; a.S = subseq(s); a.cf = s->capacity_factor;
   a.status = status_word(ws);
   a.cap_keys = reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + L.cap);
+  a.cap_counts = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + L.capn);
   return a;
+}
+
+// capacity dropping: the candidate list lengths start at zero (a memset
+// ahead of the call's kernels keeps the kernels' dependent-launch chain whole)
+cudaError_t clear_capacity_counts(const moe_shape_t *s, const RouteArgs &a, cudaStream_t st) {
+  if (!s->drop) return cudaSuccess;
+  const int64_t S = subseq(s);
+  const int64_t n_sub = (s->T + S - 1) / S;
+  return cudaMemsetAsync(a.cap_counts, 0, (size_t)n_sub * s->E * sizeof(uint32_t), st);
 }
 
 }  // namespace
@@ -133,18 +143,19 @@ moe_status_t moe_route(const moe_shape_t *shape, const void *x, const void *W_r,
     return MOE_ERR_INVALID_ARG;
   if ((w_sg == nullptr) != (gate_logit == nullptr)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(W_r) || !aligned16(ws) || !aligned4(logits)) return MOE_ERR_INVALID_ARG;
+  if (shape->drop && subseq(shape) >= (int64_t(1) << 29)) return MOE_ERR_UNSUPPORTED;
   RouteArgs a = route_args(shape, ws);
   a.x = x; a.W_r = W_r; a.b_r = b_r; a.w_sg = w_sg; a.logits = logits; a.gate_logit = gate_logit;
   a.topk_idx = topk_idx; a.topk_prob = topk_prob; a.topk_w = topk_w; a.keep = keep;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e;
+  cudaError_t e = clear_capacity_counts(shape, a, s);
+  if (e != cudaSuccess) return cuda_status(e);
   if (router_on_tensor_cores(shape) && (w_sg == nullptr || aligned16(w_sg))) {
-    // logits on the tensor cores, then the fp32 Top-K on those logits
-    a.rt_split = router_k_split(shape->T, shape->d);
-    if (a.rt_split > 1)
-      a.rt_part = reinterpret_cast<float *>(static_cast<char *>(ws) + layout(shape).rpart);
+    // logits on the tensor cores; softmax, Top-K and weights in its epilogue
+    // (few experts) or in the Top-K kernel
     e = launch_router_tc(a, s);
-    if (e == cudaSuccess) e = launch_topk_from_logits(a, s);
+    if (e == cudaSuccess && !router_routes_in_epilogue(shape->T, shape->d, shape->E, w_sg != nullptr))
+      e = launch_topk_from_logits(a, s);
   } else {
     e = launch_router_fused(a, s);
   }
@@ -159,11 +170,13 @@ moe_status_t moe_route_topk(const moe_shape_t *shape, const float *logits, int32
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!logits || !topk_idx || !topk_prob || !topk_w || !keep || !ws || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
+  if (shape->drop && subseq(shape) >= (int64_t(1) << 29)) return MOE_ERR_UNSUPPORTED;
   RouteArgs a = route_args(shape, ws);
   a.logits = const_cast<float *>(logits);
   a.topk_idx = topk_idx; a.topk_prob = topk_prob; a.topk_w = topk_w; a.keep = keep;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_topk_from_logits(a, s);
+  cudaError_t e = clear_capacity_counts(shape, a, s);
+  if (e == cudaSuccess) e = launch_topk_from_logits(a, s);
   if (e == cudaSuccess && shape->drop) e = launch_capacity(a, s);
   return cuda_status(e);
 }
@@ -173,9 +186,9 @@ moe_status_t moe_permute(const moe_shape_t *shape, const void *x, const int32_t 
                          int32_t *counts, int32_t *offsets, void *ws, moe_stream_t stream) {
   NvtxRange trace("moe_permute");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
-  if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets || !ws)
+  if (!x || !topk_idx || !keep || !row_of || !src_of || !counts || !offsets || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(Xp) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (Xp && !aligned16(Xp)) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   PermuteArgs a{};
   a.T = shape->T; a.d = shape->d; a.E = shape->E; a.K = shape->K; a.dtype = shape->dtype;
   a.x = x; a.topk_idx = topk_idx; a.keep = keep; a.Xp = Xp; a.row_of = row_of; a.src_of = src_of;
@@ -198,9 +211,9 @@ moe_status_t moe_permute_padded(const moe_shape_t *shape, const void *x, const i
   NvtxRange trace("moe_permute_padded");
   if (!shape_ok(shape)) return MOE_ERR_INVALID_ARG;
   if (!shape->drop) return MOE_ERR_UNSUPPORTED;   // dropless routing has no fixed capacity
-  if (!x || !topk_idx || !keep || !Xp || !row_of || !src_of || !counts || !offsets || !ws)
+  if (!x || !topk_idx || !keep || !row_of || !src_of || !counts || !offsets || !ws)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(Xp) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (Xp && !aligned16(Xp)) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   const int64_t C = moe_padded_capacity(shape);
   if (C <= 0) return MOE_ERR_UNSUPPORTED;
   PermuteArgs a{};
@@ -258,6 +271,28 @@ moe_status_t moe_expert_ffn(int32_t dtype, int64_t max_rows, int32_t d, int32_t 
   a.H_save = H_save; a.Yp = Yp; a.status = status_word(ws);
   cudaStream_t s = (cudaStream_t)stream;
   return cuda_status(dtype == MOE_BF16 ? launch_ffn_fwd_bf16(a, s) : launch_ffn_fwd_f32(a, s));
+}
+
+moe_status_t moe_expert_ffn_gather(int64_t max_rows, int32_t d, int32_t F, int32_t n_groups,
+                                   const int32_t *offsets, const void *x, int64_t T, int32_t K,
+                                   const int32_t *src_of, const void *W_gu, const void *W_down,
+                                   void *A_save, void *H_save, void *Yp, void *ws,
+                                   moe_stream_t stream) {
+  NvtxRange trace("moe_expert_ffn_gather");
+  moe_status_t st = ffn_check(MOE_BF16, max_rows, d, F, n_groups, offsets, ws);
+  if (st != MOE_OK) return st;
+  if (T < 1 || K < 1 || K > 8 || T * (int64_t)K >= (int64_t(1) << 31)) return MOE_ERR_INVALID_ARG;
+  if (!x || !src_of || !W_gu || !W_down || !H_save || !Yp) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_gu) || !aligned16(W_down) || !aligned16(H_save) ||
+      !aligned16(Yp) || (A_save && !aligned16(A_save)))
+    return MOE_ERR_INVALID_ARG;
+  FfnArgs a{};
+  a.dtype = MOE_BF16; a.max_rows = max_rows; a.d = d; a.F = F; a.n_groups = n_groups;
+  a.offsets = offsets; a.W_gu = W_gu; a.W_down = W_down; a.A_save = A_save;
+  a.H_save = H_save; a.Yp = Yp; a.status = status_word(ws);
+  a.x = x; a.src_of = src_of; a.K = K; a.T = T;
+  const cudaError_t e = launch_ffn_fwd_bf16(a, (cudaStream_t)stream);
+  return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : cuda_status(e);
 }
 
 moe_status_t moe_unpermute(const moe_shape_t *shape, const void *Yp, const int32_t *row_of,

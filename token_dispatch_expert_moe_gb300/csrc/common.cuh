@@ -127,12 +127,8 @@ struct RouteArgs {
   float *topk_prob, *topk_w;
   uint8_t *keep;
   uint32_t *status;
-  unsigned long long *cap_keys;  // ws region for capacity candidates
-  uint32_t *cap_count;           // ws region, one counter per (sub-seq, expert)
-  // tensor-core logits with a split K loop: rt_split partial sums
-  // [rt_split][T][E + (w_sg != null)] that the Top-K kernel adds in split order
-  int rt_split;                  // <= 1: no split (logits written directly)
-  float *rt_part;                // ws region
+  unsigned long long *cap_keys;  // ws region: capacity candidate lists [n_sub][E][S]
+  uint32_t *cap_counts;          // ws region: list lengths [n_sub][E], zeroed by the call
 };
 
 constexpr int kRouterMaxSplit = 4;
@@ -142,7 +138,12 @@ int router_k_split(int64_t T, int d);
 
 cudaError_t launch_router_fused(const RouteArgs &a, cudaStream_t s);
 cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s);  // bf16, d % 64 == 0
+// whether launch_router_tc also routes (softmax, Top-K, weights); if not,
+// launch_topk_from_logits follows it
+bool router_routes_in_epilogue(int64_t T, int d, int E, int has_gate);
 cudaError_t launch_topk_from_logits(const RouteArgs &a, cudaStream_t s);
+// capacity dropping (drop = 1): a.cap_counts must be zero (moe_route and
+// moe_route_topk clear it with a memset before their first kernel)
 cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s);
 
 struct PermuteArgs {
@@ -193,6 +194,12 @@ struct FfnArgs {
   void *dA;
   float *dXp, *dW_gu, *dW_down;
   void *H_tmp;  // fwd scratch for H when H_save is NULL (ws)
+  // fwd, bf16: when x is set, the gate/up GEMM gathers its A rows from x
+  // [T, d] through src_of (row R is token src_of[R] / K) instead of reading Xp
+  const void *x;
+  const int32_t *src_of;
+  int K;
+  int64_t T;
   void *maps;   // bwd (bf16): kFfnMapBytes of workspace, 128-byte aligned, for group tensor maps
   uint32_t *status;
 };

@@ -19,6 +19,8 @@
 //      Rows come out expert-major and token-ascending.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -26,10 +28,13 @@ namespace {
 
 constexpr int kMapBlock = 256;  // tokens per map CTA (8 words of 32 bits)
 
-// Programmatic dependent launch: the map scatter and the row copy are
-// launched while their predecessor still runs; each waits for it (and its
-// memory) at griddepcontrol.wait before reading what it wrote. Inputs written
-// before the whole call (x, topk_idx, keep) may be read before the wait.
+// Programmatic dependent launch: the map count, the map scatter and the row
+// copy are launched while their predecessor still runs; each waits for it
+// (and its memory) at griddepcontrol.wait before reading what it wrote. The
+// map count waits before it reads topk_idx and keep (the router's last kernel
+// may still be writing them) and lets its dependents launch only after that
+// wait, so the later kernels may read x, topk_idx and keep before their own
+// wait: whatever wrote those had completed when the map count passed its.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -37,9 +42,10 @@ __device__ __forceinline__ void pdl_trigger() {
 
 __global__ void __launch_bounds__(kMapBlock) map_count_kernel(PermuteArgs a) {
   extern __shared__ uint32_t bm[];  // [E][8]
-  pdl_trigger();
   const int E = a.E, K = a.K;
   for (int i = threadIdx.x; i < E * 8; i += blockDim.x) bm[i] = 0;
+  pdl_wait();   // topk_idx and keep may come from the router's last kernel
+  pdl_trigger();   // after the wait: the later kernels read x before theirs
   __syncthreads();
   const int64_t t = (int64_t)blockIdx.x * kMapBlock + threadIdx.x;
   if (t < a.T) {
@@ -201,46 +207,58 @@ __global__ void __launch_bounds__(256) pad_fill_kernel(PermuteArgs a, int vec_pe
   const int e = blockIdx.x;
   const int64_t lo = (int64_t)e * a.pad_rows + a.counts[e], hi = (int64_t)(e + 1) * a.pad_rows;
   uint4 *Xp = static_cast<uint4 *>(a.Xp);
-  for (int64_t i = lo * vec_per_row + threadIdx.x; i < hi * vec_per_row; i += blockDim.x)
-    Xp[i] = make_uint4(0, 0, 0, 0);
+  if (Xp != nullptr)
+    for (int64_t i = lo * vec_per_row + threadIdx.x; i < hi * vec_per_row; i += blockDim.x)
+      Xp[i] = make_uint4(0, 0, 0, 0);
   for (int64_t r = lo + threadIdx.x; r < hi; r += blockDim.x) a.src_of[r] = -1;
 }
 
 // out[t] = sum_k w[t,k] Yp[row_of[t,k]] (+ sigmoid(z_t) Ys[t]), fp32 sum in
-// slot order, one rounding to T.
-template <typename T>
+// slot order, one rounding to T. KK >= K is a compile-time slot bound, so
+// that per 16-byte column vector all K row loads (and the Ys load) are issued
+// before the first use: K + 1 loads per thread in flight.
+template <typename T, int KK, bool SHARED>
 __global__ void __launch_bounds__(256) unpermute_kernel(UnpermuteArgs a) {
   constexpr int N = Vec<T>::N;
   const int64_t t = blockIdx.x;
   const int K = a.K;
-  __shared__ int32_t rows[8];
-  __shared__ float wts[8];
+  __shared__ int32_t rows[KK];
+  __shared__ float wts[KK];
   __shared__ float gate;
-  if (threadIdx.x < K) {
-    rows[threadIdx.x] = a.row_of[t * K + threadIdx.x];
-    wts[threadIdx.x] = a.topk_w[t * K + threadIdx.x];
+  if (threadIdx.x < KK) {
+    const bool in = threadIdx.x < K;
+    rows[threadIdx.x] = in ? a.row_of[t * K + threadIdx.x] : -1;
+    wts[threadIdx.x] = in ? a.topk_w[t * K + threadIdx.x] : 0.0f;
   }
-  if (threadIdx.x == 0 && a.Ys != nullptr) gate = 1.0f / (1.0f + __expf(-a.gate_logit[t]));
+  if (SHARED && threadIdx.x == 0) gate = 1.0f / (1.0f + __expf(-a.gate_logit[t]));
   __syncthreads();
   const T *Yp = reinterpret_cast<const T *>(a.Yp);
   const T *Ys = reinterpret_cast<const T *>(a.Ys);
   T *out = reinterpret_cast<T *>(a.out);
+  int32_t r[KK];
+#pragma unroll
+  for (int k = 0; k < KK; ++k) r[k] = rows[k];
   for (int v = threadIdx.x * N; v < a.d; v += blockDim.x * N) {
+    uint4 yraw[KK + 1];
+#pragma unroll
+    for (int k = 0; k < KK; ++k)
+      if (r[k] >= 0) yraw[k] = *reinterpret_cast<const uint4 *>(Yp + (int64_t)r[k] * a.d + v);
+    if constexpr (SHARED) yraw[KK] = *reinterpret_cast<const uint4 *>(Ys + t * a.d + v);
     float acc[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const int32_t r = rows[k];
-      if (r < 0) continue;
+#pragma unroll
+    for (int k = 0; k < KK; ++k) {
+      if (r[k] < 0) continue;
       float y[N];
-      load16<T>(Yp + (int64_t)r * a.d + v, y);
+      unpack16<T>(yraw[k], y);
       const float w = wts[k];
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = fmaf(w, y[i], acc[i]);
     }
-    if (Ys != nullptr) {
+    if constexpr (SHARED) {
       float y[N];
-      load16<T>(Ys + t * a.d + v, y);
+      unpack16<T>(yraw[KK], y);
 #pragma unroll
       for (int i = 0; i < N; ++i) acc[i] = fmaf(gate, y[i], acc[i]);
     }
@@ -250,69 +268,78 @@ __global__ void __launch_bounds__(256) unpermute_kernel(UnpermuteArgs a) {
 
 // dYp[row] = w * dout[t]; dw[t,k] = <dout[t], Yp[row]>; shared: dYs, dz.
 // One CTA per token. Per 16-byte column vector a thread first issues the
-// loads of all K expert rows (and Ys), then computes and stores, so that up to
-// K + 2 loads per thread are in flight. The K (+1) dot products are reduced
-// with one butterfly per warp and then over the warps in order (fixed order:
-// bitwise reproducible).
-template <typename T>
+// loads of all K expert rows (and Ys), then computes and stores, so that
+// K + 2 loads per thread are in flight; KK >= K is a compile-time bound,
+// which keeps the registers per thread (and so the CTAs per SM) in line
+// with the actual K. The K (+1) dot products are reduced with one butterfly
+// per warp and then over the warps in order (fixed order: bitwise
+// reproducible).
+template <typename T, int KK, bool SHARED>
 __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
   constexpr int N = Vec<T>::N;
+  constexpr int NS = KK + (SHARED ? 1 : 0);   // dot products per token
   const int64_t t = blockIdx.x;
   const int K = a.K;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ int32_t rows[8];
-  __shared__ float wts[8];
+  __shared__ int32_t rows[KK];
+  __shared__ float wts[KK];
   __shared__ float gate;
-  __shared__ float red[8][9];   // [warp][slot]; slot 8 = shared expert
-  if (threadIdx.x < K) {
-    rows[threadIdx.x] = a.row_of[t * K + threadIdx.x];
-    wts[threadIdx.x] = a.topk_w[t * K + threadIdx.x];
+  __shared__ float red[8][NS];   // [warp][slot]; slot KK = shared expert
+  if (threadIdx.x < KK) {
+    const bool in = threadIdx.x < K;
+    rows[threadIdx.x] = in ? a.row_of[t * K + threadIdx.x] : -1;
+    wts[threadIdx.x] = in ? a.topk_w[t * K + threadIdx.x] : 0.0f;
   }
-  if (threadIdx.x == 0 && a.Ys != nullptr) gate = 1.0f / (1.0f + __expf(-a.gate_logit[t]));
+  if (SHARED && threadIdx.x == 0) gate = 1.0f / (1.0f + __expf(-a.gate_logit[t]));
   __syncthreads();
-  const bool shared = a.Ys != nullptr;
   const T *Yp = reinterpret_cast<const T *>(a.Yp);
   const T *dout = reinterpret_cast<const T *>(a.dout);
   T *dYp = reinterpret_cast<T *>(a.dYp);
-  float dot[9];
+  int32_t r[KK];
+  float wk[KK];
 #pragma unroll
-  for (int k = 0; k < 9; ++k) dot[k] = 0.0f;
+  for (int k = 0; k < KK; ++k) {
+    r[k] = rows[k];
+    wk[k] = wts[k];
+  }
+  float dot[NS];
+#pragma unroll
+  for (int k = 0; k < NS; ++k) dot[k] = 0.0f;
   for (int v = threadIdx.x * N; v < a.d; v += blockDim.x * N) {
-    uint4 graw, yraw[9];
-    graw = *reinterpret_cast<const uint4 *>(dout + t * a.d + v);
+    uint4 yraw[NS];
+    const uint4 graw = *reinterpret_cast<const uint4 *>(dout + t * a.d + v);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < K && rows[k] >= 0)
-        yraw[k] = *reinterpret_cast<const uint4 *>(Yp + (int64_t)rows[k] * a.d + v);
-    if (shared) yraw[8] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.Ys) + t * a.d + v);
+    for (int k = 0; k < KK; ++k)
+      if (r[k] >= 0) yraw[k] = *reinterpret_cast<const uint4 *>(Yp + (int64_t)r[k] * a.d + v);
+    if constexpr (SHARED)
+      yraw[KK] = *reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(a.Ys) + t * a.d + v);
     float g[N];
     unpack16<T>(graw, g);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k >= K || rows[k] < 0) continue;
+    for (int k = 0; k < KK; ++k) {
+      if (r[k] < 0) continue;
       float y[N], o[N];
       unpack16<T>(yraw[k], y);
-      const float w = wts[k];
 #pragma unroll
       for (int i = 0; i < N; ++i) {
         dot[k] = fmaf(g[i], y[i], dot[k]);
-        o[i] = w * g[i];
+        o[i] = wk[k] * g[i];
       }
-      store16<T>(dYp + (int64_t)rows[k] * a.d + v, o);
+      store16<T>(dYp + (int64_t)r[k] * a.d + v, o);
     }
-    if (shared) {
+    if constexpr (SHARED) {
       float y[N], o[N];
-      unpack16<T>(yraw[8], y);
+      unpack16<T>(yraw[KK], y);
 #pragma unroll
       for (int i = 0; i < N; ++i) {
-        dot[8] = fmaf(g[i], y[i], dot[8]);
+        dot[KK] = fmaf(g[i], y[i], dot[KK]);
         o[i] = gate * g[i];
       }
       store16<T>(reinterpret_cast<T *>(a.dYs) + t * a.d + v, o);
     }
   }
 #pragma unroll
-  for (int k = 0; k < 9; ++k) {
+  for (int k = 0; k < NS; ++k) {
     const float s = warp_sum(dot[k]);
     if (lane == 0) red[warp][k] = s;
   }
@@ -323,9 +350,9 @@ __global__ void __launch_bounds__(256) unpermute_bwd_kernel(UnpermuteArgs a) {
     float s = 0.0f;
     for (int w = 0; w < nw; ++w) s += red[w][k];
     a.dw[t * K + k] = rows[k] >= 0 ? s : 0.0f;
-  } else if (threadIdx.x == 32 && shared) {
+  } else if (SHARED && threadIdx.x == 32) {
     float s = 0.0f;
-    for (int w = 0; w < nw; ++w) s += red[w][8];
+    for (int w = 0; w < nw; ++w) s += red[w][NS - 1];
     a.dz[t] = gate * (1.0f - gate) * s;
   }
 }
@@ -390,26 +417,56 @@ constexpr int kNoAllocBlocks = MOE_PERMUTE_NOALLOC_MAX_TOKENS / kMapBlock;
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocBlocks * 64];
 
 namespace {
-constexpr int kMaxDevices = 64;
+// Device address of g_permute_scratch in the current context. In host code
+// the array's name is only a handle, so the address is looked up with
+// cudaGetSymbolAddress (with the device current) the first time a context
+// calls, and cached under the context's unique ID (cuCtxGetId: never reused
+// within the process, so a context created after cudaDeviceReset, where the
+// module and its array are loaded again, gets a lookup of its own).
+constexpr int kMaxContexts = 64;
 std::mutex g_scratch_mutex;
-int32_t *g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxContexts] = {};
+int32_t *g_scratch_addr[kMaxContexts] = {};
+int g_scratch_n = 0;
 
-// Device address of g_permute_scratch on the current device. In host code the
-// array's name is only a handle, so the address is looked up once per device
-// (cudaGetSymbolAddress, with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name, int version) {
+  void *ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(ptr);
+}
+
 cudaError_t permute_scratch(int32_t **out) {
-  int dev = 0;
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (get_current == nullptr || get_id == nullptr) return cudaErrorNotSupported;
+  int dev = 0;   // cudaSetDevice makes the device's primary context current on this thread
   cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return cudaErrorNotSupported;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_permute_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = static_cast<int32_t *>(p);
-  }
-  *out = g_scratch_addr[dev];
+  for (int i = 0; i < g_scratch_n; ++i)
+    if (g_scratch_ctx[i] == id) {
+      *out = g_scratch_addr[i];
+      return cudaSuccess;
+    }
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_permute_scratch);
+  if (e != cudaSuccess) return e;
+  const int slot = g_scratch_n < kMaxContexts ? g_scratch_n++ : (int)(id % kMaxContexts);
+  g_scratch_ctx[slot] = id;
+  g_scratch_addr[slot] = static_cast<int32_t *>(p);
+  *out = static_cast<int32_t *>(p);
   return cudaSuccess;
 }
 }  // namespace
@@ -427,7 +484,6 @@ cudaError_t launch_permute_noalloc(PermuteArgs a, cudaStream_t s) {
 cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   const int nblk = (int)((a.T + kMapBlock - 1) / kMapBlock);
   const size_t bm_bytes = (size_t)a.E * 8 * sizeof(uint32_t);
-  map_count_kernel<<<nblk, kMapBlock, bm_bytes, s>>>(a);
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -438,8 +494,10 @@ cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, map_scatter_kernel, a, nblk);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, map_count_kernel, a);
   if (e != cudaSuccess) return e;
+  e = cudaLaunchKernelEx(&cfg, map_scatter_kernel, a, nblk);
+  if (e != cudaSuccess || a.Xp == nullptr) return e;   // Xp NULL: the map alone
   const uint32_t row_bytes = (uint32_t)a.d * (a.dtype == MOE_BF16 ? 2u : 4u);
   int tpc = kPermTokens;
   while (tpc > 1 && (uint32_t)tpc * row_bytes > kPermSmemCap) --tpc;
@@ -454,20 +512,43 @@ cudaError_t launch_permute(const PermuteArgs &a, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, permute_bulk_kernel, a, row_bytes, tpc);
 }
 
-cudaError_t launch_unpermute(const UnpermuteArgs &a, cudaStream_t s) {
-  if (a.dtype == MOE_BF16)
-    unpermute_kernel<__nv_bfloat16><<<(unsigned)a.T, 256, 0, s>>>(a);
+// Slot bound KK >= K of the un-permute kernels: 1, 2, 4 or 8.
+template <typename T, int KK>
+cudaError_t launch_unpermute_kk(const UnpermuteArgs &a, cudaStream_t s) {
+  if (a.Ys != nullptr)
+    unpermute_kernel<T, KK, true><<<(unsigned)a.T, 256, 0, s>>>(a);
   else
-    unpermute_kernel<float><<<(unsigned)a.T, 256, 0, s>>>(a);
+    unpermute_kernel<T, KK, false><<<(unsigned)a.T, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute_bwd(const UnpermuteArgs &a, cudaStream_t s) {
-  if (a.dtype == MOE_BF16)
-    unpermute_bwd_kernel<__nv_bfloat16><<<(unsigned)a.T, 256, 0, s>>>(a);
+template <typename T, int KK>
+cudaError_t launch_unpermute_bwd_kk(const UnpermuteArgs &a, cudaStream_t s) {
+  if (a.Ys != nullptr)
+    unpermute_bwd_kernel<T, KK, true><<<(unsigned)a.T, 256, 0, s>>>(a);
   else
-    unpermute_bwd_kernel<float><<<(unsigned)a.T, 256, 0, s>>>(a);
+    unpermute_bwd_kernel<T, KK, false><<<(unsigned)a.T, 256, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_unpermute_t(const UnpermuteArgs &a, cudaStream_t s, bool bwd) {
+  if (a.K <= 1) return bwd ? launch_unpermute_bwd_kk<T, 1>(a, s) : launch_unpermute_kk<T, 1>(a, s);
+  if (a.K <= 2) return bwd ? launch_unpermute_bwd_kk<T, 2>(a, s) : launch_unpermute_kk<T, 2>(a, s);
+  if (a.K <= 4) return bwd ? launch_unpermute_bwd_kk<T, 4>(a, s) : launch_unpermute_kk<T, 4>(a, s);
+  return bwd ? launch_unpermute_bwd_kk<T, 8>(a, s) : launch_unpermute_kk<T, 8>(a, s);
+}
+
+cudaError_t launch_unpermute(const UnpermuteArgs &a, cudaStream_t s) {
+  if (a.K < 1 || a.K > 8) return cudaErrorInvalidValue;
+  return a.dtype == MOE_BF16 ? launch_unpermute_t<__nv_bfloat16>(a, s, false)
+                             : launch_unpermute_t<float>(a, s, false);
+}
+
+cudaError_t launch_unpermute_bwd(const UnpermuteArgs &a, cudaStream_t s) {
+  if (a.K < 1 || a.K > 8) return cudaErrorInvalidValue;
+  return a.dtype == MOE_BF16 ? launch_unpermute_t<__nv_bfloat16>(a, s, true)
+                             : launch_unpermute_t<float>(a, s, true);
 }
 
 cudaError_t launch_pad_fill(const PermuteArgs &a, cudaStream_t s) {

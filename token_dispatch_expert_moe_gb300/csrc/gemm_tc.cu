@@ -54,6 +54,7 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "softmax.cuh"
 
 namespace moe {
 namespace {
@@ -64,6 +65,9 @@ constexpr int kStages = 4;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kThreads = 192;
+constexpr int kGatherWarps = 2;   // A-gather warps (GU gather mode): 256 threads in all, so
+                                  // the epilogue keeps the registers it has without them
+constexpr int kThreadsGather = kThreads + 32 * kGatherWarps;
 constexpr int kABytes = BM * BK * 2;          // 16 KB
 constexpr int kBBytesMax = 256 * BK * 2;      // 32 KB
 constexpr int kStageBytes = kABytes + kBBytesMax;
@@ -78,6 +82,7 @@ struct TcParams {
   CUtensorMap tmC;   // RT: the gate vector w_sg as a [1, d] tensor
   CUtensorMap tmO0;  // bulk-store map of out0 (box: 32 rows x 128 bytes)
   CUtensorMap tmO1;  // bulk-store map of out1 (GU: A_save)
+  CUtensorMap tmX;   // GU gather: x [T, d] in boxes of one row x 64 columns
   int mode;
   int n_groups;
   int64_t max_rows;
@@ -95,13 +100,23 @@ struct TcParams {
   // zero-fills the K rows past the group's end of a ragged last K block
   const CUtensorMap *gmaps;
   int fault_stall;   // test hook: the producer issues no loads (waits run out)
-  // RT
+  // GU with a gathered A operand (the permutation fused into the GEMM): row
+  // R < offsets[n_groups] of the tile is token src_of[R] / gK of x [gT, d]
+  // (through tmX); other rows, and rows with src_of < 0 (padding), are zero
+  const int32_t *src_of;
+  int gK;
+  int64_t gT;
+  // RT: logits, then softmax, Top-K and combine weights in the epilogue
   int64_t T;
   int E, e_pad, has_gate;
   const float *bias;
   float *gate_out;
-  int k_split, kb_per;  // K blocks split over k_split tiles of kb_per blocks each
-  float *part;          // k_split > 1: partial sums [k_split][T][E + has_gate]
+  int k_split, kb_per;  // K blocks split over k_split tiles of kb_per blocks each;
+                        // k_split > 1: the split tiles of a row tile form a cluster
+  int K, renorm, ep;    // Top-K, renormalisation; ep: 0 (logits only) or 8/16 >= E
+  int32_t *topk_idx;
+  float *topk_prob, *topk_w;
+  uint8_t *keep;
   uint32_t *status;
 };
 
@@ -128,6 +143,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+// try_wait with acquire at cluster scope: pairs with release arrivals that
+// the other CTA of a pair makes on this barrier
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// arrive on a barrier of either CTA of the pair (cluster address), raising
+// its expected transaction bytes first
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_addr),
+               "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -347,6 +383,7 @@ struct SharedState {
   uint64_t tempty[2];
   uint64_t drain;
   uint64_t ebar[4];  // DH: per-epilogue-warp A_save box loads
+  uint64_t xbar;     // RT with a split K loop: the other parts' partial logits arrived
   uint32_t tmem_base;
   volatile int abort;
   int total_tiles;
@@ -388,13 +425,16 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, const SharedState
 }
 
 __device__ bool wait_bounded(SharedState &st, uint32_t bar, uint32_t parity, uint32_t *status,
-                             uint32_t role) {
-  if (mbar_try_wait(bar, parity)) return true;
+                             uint32_t role, bool cluster_acquire = false) {
+  auto test = [&]() {
+    return cluster_acquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (test()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (test()) return true;
     if (st.abort) return false;
     if (globaltimer() - t0 > kTimeoutNs) {
       report(status, MOE_ERR_TIMEOUT, kInfoGemmTimeout + role);
@@ -404,36 +444,145 @@ __device__ bool wait_bounded(SharedState &st, uint32_t bar, uint32_t parity, uin
   }
 }
 
+// Router epilogue, one token row per thread: bias, logits out, then the
+// routing softmax, Top-K and combine weights in the fp32 arithmetic that
+// softmax.cuh specifies for a warp, done here by one thread over its row:
+// the same maximum, the same exponential of each difference, the sum in the
+// same pairwise tree (zero-padded to EP, a power of two >= E: adding the zero
+// padding is exact, so any such EP gives the tree of the next power of two),
+// correctly rounded divisions, K arg-max rounds with ties to the lower
+// expert, Z summed in slot order. v holds the row's fp32 sums (columns < E,
+// the gate logit, when present, at column GC = the tile width - 16).
+template <int EP, int NV, int GC>
+__device__ __forceinline__ void route_row(const TcParams &p, const float (&v)[NV], int64_t row) {
+  const int E = p.E;
+  float l[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    l[e] = v[e];
+    if (e < E && p.bias != nullptr) l[e] = __fadd_rn(l[e], p.bias[e]);
+  }
+  float *lg = reinterpret_cast<float *>(p.out0) + row * E;
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e < E) lg[e] = l[e];
+  if (p.has_gate) p.gate_out[row] = v[GC];
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e < E) m = fmaxf(m, l[e]);
+  float q[EP], sum[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) {
+    q[e] = e < E ? spec::exp_spec(__fsub_rn(l[e], m)) : 0.0f;
+    sum[e] = q[e];
+  }
+#pragma unroll
+  for (int lv = 1; lv <= 6; ++lv) {   // h = EP/2, EP/4, ..., 1 (constant bounds: registers)
+    const int h = EP >> lv;
+#pragma unroll
+    for (int i = 0; i < EP / 2; ++i)
+      if (i < h) sum[i] = __fadd_rn(sum[i], sum[i + h]);
+  }
+  float pr[EP];
+#pragma unroll
+  for (int e = 0; e < EP; ++e) pr[e] = e < E ? __fdiv_rn(q[e], sum[0]) : -1.0f;
+  float bp[8];
+  int bi[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    bp[k] = 0.0f;
+    bi[k] = 0;
+    if (k < p.K) {
+      float b = -3.0f;
+      int ix = 0;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (pr[e] > b) { b = pr[e]; ix = e; }
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e == ix) pr[e] = -2.0f;
+      bp[k] = b;
+      bi[k] = ix;
+    }
+  }
+  float Z = bp[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k)
+    if (k < p.K) Z = __fadd_rn(Z, bp[k]);
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < p.K) {
+      p.topk_idx[row * p.K + k] = bi[k];
+      p.topk_prob[row * p.K + k] = bp[k];
+      p.topk_w[row * p.K + k] = p.renorm ? __fdiv_rn(bp[k], Z) : bp[k];
+      p.keep[row * p.K + k] = 1;
+    }
+}
+
 // One tile's epilogue for the epilogue warp that owns TMEM lane quarter q.
+// xbuf (router mode with a split K loop, even CTA): the other parts' partial
+// sums, [part - 1][128 rows][E + has_gate].
 template <int MODE, int BN>
 __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st, Stager &sg,
                                               uint32_t &ephase, const Tile &t, uint32_t tbase,
-                                              int q, int warp, int lane) {
+                                              int q, int warp, int lane, float *xbuf = nullptr) {
   using TR = ModeTraits<MODE>;
   const int r_loc = t.m * BM + q * 32 + lane;
   if constexpr (MODE == RT) {
+    constexpr int NV = (BN + 31) / 32 * 32;
+    constexpr int GC = BN - 16;   // the gate logit's column (tile width = E rounded to 16, + 16)
+    const int rl = q * 32 + lane;   // row within the tile
     const int64_t row = r_loc;
     const bool valid = row < p.T;
-    const bool split = p.k_split > 1;
     const int C = p.E + p.has_gate;
-    float *lg = split ? p.part + ((int64_t)t.n * p.T + row) * C
-                      : reinterpret_cast<float *>(p.out0) + row * p.E;
-#pragma unroll 1
-    for (int c = 0; c < (BN + 31) / 32; ++c) {
-      float v[32];
-      tmem_ld32(tbase + c * 32, v);
-      if (valid) {
+    float v[NV];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = c * 32 + i;
-          if (e < p.E) lg[e] = (!split && p.bias != nullptr) ? __fadd_rn(v[i], p.bias[e]) : v[i];
-          if (p.has_gate && e == p.e_pad) {
-            if (split) lg[p.E] = v[i];
-            else p.gate_out[row] = v[i];
+    for (int c = 0; c < NV / 32; ++c) {
+      float chunk[32];
+      tmem_ld32(tbase + c * 32, chunk);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[c * 32 + i] = chunk[i];
+    }
+    if (p.k_split > 1) {
+      // part t.n of the K loop; part 0 (the even CTA of the cluster) adds the
+      // others in part order
+      if (t.n != 0) {
+        if (valid) {
+          const uint32_t dst = map_to_cta(smem_u32(xbuf + ((t.n - 1) * BM + rl) * C), 0);
+#pragma unroll
+          for (int j = 0; j < NV; ++j) {
+            const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
+            if (e >= 0)
+              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * e), "f"(v[j]) : "memory");
           }
+        }
+        mbar_arrive_cluster(map_to_cta(smem_u32(&st.xbar), 0));
+        return;
+      }
+      if (!wait_bounded(st, smem_u32(&st.xbar), 0, p.status, 7, true)) return;
+      if (!valid) return;
+      for (int part = 1; part < p.k_split; ++part) {
+        const float *src = xbuf + ((part - 1) * BM + rl) * C;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
+          if (e >= 0) v[j] = __fadd_rn(v[j], src[e]);
         }
       }
     }
+    if (!valid) return;
+    if (p.ep == 0) {   // logits only: the Top-K kernel routes
+      float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[e], p.bias[e]) : v[e];
+      }
+      if (p.has_gate) p.gate_out[row] = v[GC];
+      return;
+    }
+    if (p.ep == 8) route_row<8, NV, GC>(p, v, row);
+    else route_row<16, NV, GC>(p, v, row);
   } else if constexpr (TR::red) {
     // weight-gradient tiles are always whole: bulk stores of 32 x 32 fp32
     const bool empty = t.rows <= 0;
@@ -660,19 +809,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
   constexpr uint32_t kStageTx = kABytes + MMA_N * BK * 2;
   constexpr uint32_t kIdesc = instr_desc(BM, MMA_N, TR::a_mn, TR::b_mn);
-  // the router's B operand is at most 80 rows (10 KB): six 32 KB stages in
-  // the space of four 48 KB ones keep more of x in flight
+  // the router's B operand is at most 80 rows (10 KB): six stages of 16 KB
+  // of x and the B rows (rounded to 1 KB, the 128-byte swizzle atom) keep more
+  // of x in flight; the space after the ring holds the K-split exchange
   constexpr int NST = MODE == RT ? 6 : kStages;
-  constexpr int SBYTES = MODE == RT ? kABytes + 16384 : kStageBytes;
+  constexpr int SBYTES = MODE == RT ? kABytes + (BN * BK * 2 + 1023) / 1024 * 1024 : kStageBytes;
   static_assert(NST * SBYTES <= kStages * kStageBytes && NST <= kMaxStages, "ring too large");
   static_assert(MODE != RT || BN * BK * 2 <= 16384, "router B operand exceeds its stage");
 
+  // the router's Top-K kernel is launched as a programmatic dependent: it
+  // may be scheduled now and waits (griddepcontrol.wait) for this grid
+  if constexpr (MODE == RT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *staging = smem + kStages * kStageBytes;
   SharedState &st = *reinterpret_cast<SharedState *>(staging + kEpiStagingBytes);
+  float *xbuf = reinterpret_cast<float *>(smem + NST * SBYTES);   // RT K-split exchange
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool clustered = MODE == RT && p.k_split > 1;
 
   // ---- set-up: tile table, barriers, TMEM
   if (threadIdx.x == 0) {
@@ -680,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int total = 0;
     bool bad = false;
     if constexpr (MODE == RT) {
+      mbar_init(smem_u32(&st.xbar), (uint32_t)(p.k_split > 1 ? (p.k_split - 1) * BM : 1));
       total = (int)((p.T + BM - 1) / BM) * p.k_split;
     } else if constexpr (TR::red) {
       for (int g = 0; g < p.n_groups; ++g)
@@ -727,6 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
   tc_fence_before();
   __syncthreads();
+  if (clustered) cluster_sync();   // the even CTA's exchange barrier exists before any arrival
   tc_fence_after();
   const uint32_t tmem = st.tmem_base;
   const int total = st.total_tiles;
@@ -864,7 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tfull[buf]), use, p.status, 4))) break;
       tc_fence_after();
       const uint32_t tbase = tmem + buf * 256 + ((uint32_t)(q * 32) << 16);
-      epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane);
+      epilogue_tile<MODE, BN>(p, st, sg, ephase, t, tbase, q, warp, lane, xbuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&st.tempty[buf]));
@@ -876,6 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
+  if (clustered) cluster_sync();   // no CTA leaves while another may still write to it
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -926,9 +1084,11 @@ __device__ __forceinline__ Tile decode_pair_tile(const TcParams &p, const Shared
   return t;
 }
 
-template <int MODE, int BN, int NSUB>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+template <int MODE, int BN, int NSUB, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
+  static_assert(!GATHER || (MODE == GU && NSUB == 1), "the A gather serves the gate/up GEMM");
   using TR = ModeTraits<MODE>;
   constexpr int kPairStages = pair_stages<NSUB>();
   constexpr int kPairStageBytes = pair_stage_bytes<NSUB>();
@@ -937,7 +1097,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   static_assert(NSUB == 1 || HALF_N * BK * 2 == 16384, "two B halves of 16 KB per stage");
   constexpr int A_BOXES = TR::a_mn ? BM / 64 : 1;
   constexpr int B_HALF_BOXES = TR::b_mn ? HALF_N / 64 : 1;
-  constexpr uint32_t kOwnTx = kABytes + NSUB * HALF_N * BK * 2;   // one CTA's bytes per stage
+  // one CTA's TMA bytes per stage (the gathered A arrives by cp.async instead)
+  constexpr uint32_t kOwnTx = (GATHER ? 0 : kABytes) + NSUB * HALF_N * BK * 2;
   constexpr uint32_t kTx = 2u * kOwnTx;
   constexpr uint32_t kIdesc = instr_desc(256, MMA_N, TR::a_mn, TR::b_mn);
 
@@ -978,7 +1139,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     }
     st.total_tiles = total;
     for (int i = 0; i < kPairStages; ++i) {
-      mbar_init(smem_u32(&st.full[i]), 1);
+      // GATHER: + one arrival per gather warp of each CTA (with its row bytes)
+      mbar_init(smem_u32(&st.full[i]), GATHER ? 1 + 2 * kGatherWarps : 1);
       mbar_init(smem_u32(&st.empty[i]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -1042,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
                 tma_load_2d_pair(sb + j * 16384 + b * 8192, mB, bar,
                                  (t.n + j) * BN + (int)rank * HALF_N + 64 * b, kb * BK);
           } else {
-            tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
+            if constexpr (!GATHER) tma_load_2d_pair(sa, &p.tmA, bar, kb * BK, t.row0 + t.m * BM);
             const int64_t gb = (int64_t)t.g * p.b_group_rows;
 #pragma unroll
             for (int j = 0; j < NSUB; ++j) {   // B half of each of the tile's N tiles
@@ -1139,7 +1301,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp < 6) {
     // ======================= epilogue (both CTAs) =======================
     const int q = warp & 3;
     Stager sg{staging + (warp - 2) * 2 * kStageOutBytes, 0};
@@ -1167,6 +1329,58 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  } else if constexpr (GATHER) {
+    // ==================== A gather (GU, both CTAs) ====================
+    // Lane l of gather warp w loads rows r = 64 w + 2 l and r + 1 of this
+    // CTA's 128-row A box: per stage one TMA copy per row, a box of one row
+    // and 64 columns of x (128 bytes) put at byte offset 128 r of the stage,
+    // which is where the 128-byte swizzled box the MMA descriptor reads keeps
+    // row r (the swizzle is anchored to the shared-memory address, and the
+    // stage is 1024-byte aligned). A row without a source (past the last
+    // group, or a padding row) loads row -1: outside x, so the copy fills
+    // zeros. The copies complete on the even CTA's full barrier, on which
+    // lane 0 first arrives with the warp's 64 rows of bytes; the TMA
+    // completion orders the writes for the tensor core.
+    constexpr int kRows = BM / (32 * kGatherWarps);   // 2 rows per lane
+    const int gw = warp - 6;
+    const int64_t n_rows = p.offsets[p.n_groups];
+    const int64_t n_src = p.gT * p.gK;
+    int it = 0;
+    for (int pt = cid; pt < total && !st.abort; pt += ncl) {
+      const Tile t = decode_pair_tile<MODE, BN, NSUB>(p, st, pt, (int)rank);
+      int tok[kRows];
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        const int64_t R = (int64_t)t.row0 + (int64_t)t.m * BM + 64 * gw + 2 * lane + j;
+        tok[j] = -1;
+        if (R < n_rows) {
+          const int32_t so = p.src_of[R];
+          if (so >= 0 && so < n_src) tok[j] = so / p.gK;
+          else if (so >= 0) report(p.status, MOE_ERR_DEVICE, kInfoRowRange);
+        }
+      }
+      const int kblocks = p.K_fixed / BK;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const int s = it % kPairStages;
+        const uint32_t ph = (it / kPairStages) & 1;
+        const uint32_t bar = map_to_cta(smem_u32(&st.full[s]), 0);
+        bool w = true;
+        if (lane == 0) {
+          w = wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 6);
+          if (w) mbar_arrive_expect_tx_cluster(bar, 32 * kRows * 128);
+        }
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = smem_u32(smem + s * kPairStageBytes) + (64 * gw + 2 * lane) * 128;
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) tma_load_2d_pair(dst + j * 128, &p.tmX, bar, kb * BK, tok[j]);
+      }
+      if (!ok) break;
+    }
     __syncwarp();
   }
 
@@ -1276,13 +1490,18 @@ int num_sms() {
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + kEpiStagingBytes + sizeof(SharedState) + 1024;
 
-// Fault injection for tests of the timeout path: with MOE_FAULT_INJECT_STALL=1
-// the producer warp issues no loads, so the MMA warp's first wait runs out;
-// the kernel then records MOE_ERR_TIMEOUT and returns.
+#ifdef MOE_TEST_HOOKS
+// Test build only (libmoe_testhooks.so): fault injection for tests of the
+// timeout path. With MOE_FAULT_INJECT_STALL=1 the producer warp issues no
+// loads, so the MMA warp's first wait runs out; the kernel then records
+// MOE_ERR_TIMEOUT and returns. Read at every launch.
 int fault_stall() {
   const char *e = getenv("MOE_FAULT_INJECT_STALL");
   return (e != nullptr && e[0] == '1') ? 1 : 0;
 }
+#else
+constexpr int fault_stall() { return 0; }
+#endif
 
 template <int MODE, int BN>
 cudaError_t launch_mode(TcParams p, cudaStream_t s) {
@@ -1290,21 +1509,38 @@ cudaError_t launch_mode(TcParams p, cudaStream_t s) {
   auto k = tc_gemm_kernel<MODE, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (MODE == RT && p.k_split > 1) {
+    // the K parts of a row tile run as one cluster (one row tile per cluster:
+    // router_k_split keeps row tiles x parts within the SM count)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(num_sms() / p.k_split * p.k_split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.k_split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+  }
   k<<<num_sms(), kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
 
-template <int MODE, int BN, int NSUB = 1>
+template <int MODE, int BN, int NSUB = 1, bool GATHER = false>
 cudaError_t launch_pair(TcParams p, cudaStream_t s) {
   p.fault_stall = fault_stall();
-  auto k = tc_gemm_pair_kernel<MODE, BN, NSUB>;
+  auto k = tc_gemm_pair_kernel<MODE, BN, NSUB, GATHER>;
   constexpr size_t kPairSmemBytes = (size_t)pair_stages<NSUB>() * pair_stage_bytes<NSUB>() +
                                     kEpiStagingBytes + sizeof(SharedState) + 1024;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_sms() & ~1));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(GATHER ? kThreadsGather : kThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1317,8 +1553,10 @@ cudaError_t launch_pair(TcParams p, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, k, p);
 }
 
-// The row-grouped modes run as CTA pairs; MOE_GEMM_PAIR=0 selects the
-// single-CTA kernels instead (kept for comparison).
+// The row-grouped modes run as CTA pairs. In the test build
+// (libmoe_testhooks.so) MOE_GEMM_PAIR=0, read once, selects the single-CTA
+// kernels instead, so that tests can compare the two.
+#ifdef MOE_TEST_HOOKS
 bool pair_enabled() {
   static int v = -1;
   if (v < 0) {
@@ -1327,6 +1565,9 @@ bool pair_enabled() {
   }
   return v == 1;
 }
+#else
+constexpr bool pair_enabled() { return true; }
+#endif
 
 template <int MODE>
 cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
@@ -1361,6 +1602,24 @@ int router_k_split(int64_t T, int d) {
   return (kb + per - 1) / per;   // every split non-empty
 }
 
+constexpr int kRouteFuseMaxE = 16;   // the epilogue's routing serves E <= 16
+
+// K parts of the router GEMM: as many as leave no SM idle (router_k_split),
+// at most as many as the even CTA's exchange buffer (the shared memory after
+// the ring) holds partial sums for
+int router_parts(int64_t T, int d, int E, int has_gate) {
+  const int n = (E + 15) / 16 * 16 + 16 * has_gate;
+  const size_t stage = kABytes + ((size_t)n * BK * 2 + 1023) / 1024 * 1024;
+  const size_t room = (size_t)kStages * kStageBytes + kEpiStagingBytes - 6 * stage;
+  const int max_parts = 1 + (int)(room / ((size_t)BM * (E + has_gate) * sizeof(float)));
+  const int split = router_k_split(T, d);
+  return split < max_parts ? split : max_parts;
+}
+
+bool router_routes_in_epilogue(int64_t T, int d, int E, int has_gate) {
+  return E <= kRouteFuseMaxE && router_parts(T, d, E, has_gate) == 1;
+}
+
 cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
   const int e_pad = (a.E + 15) / 16 * 16;
   const int has_gate = a.w_sg != nullptr ? 1 : 0;
@@ -1372,12 +1631,17 @@ cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
   p.mode = RT; p.n_groups = 1; p.max_rows = a.T; p.d = a.d; p.K_fixed = a.d; p.N = n;
   p.T = a.T; p.E = a.E; p.e_pad = e_pad; p.has_gate = has_gate; p.bias = a.b_r;
   p.out0 = a.logits; p.gate_out = a.gate_logit; p.status = a.status;
+  p.K = a.K; p.renorm = a.renorm;
+  p.ep = 0;   // set below once the K split is known
+  p.topk_idx = a.topk_idx; p.topk_prob = a.topk_prob; p.topk_w = a.topk_w; p.keep = a.keep;
   const int kb = a.d / BK;
-  p.k_split = a.rt_split > 1 ? a.rt_split : 1;
-  p.kb_per = (kb + p.k_split - 1) / p.k_split;
-  if (p.k_split > 1 && (a.rt_part == nullptr || (p.k_split - 1) * p.kb_per >= kb))
-    return cudaErrorInvalidValue;
-  p.part = a.rt_part;
+  const int split = router_parts(a.T, a.d, a.E, has_gate);
+  p.kb_per = (kb + split - 1) / split;
+  p.k_split = (kb + p.kb_per - 1) / p.kb_per;   // every part non-empty
+  // routing in the epilogue (one thread per token row) when the K loop is not
+  // split and E is small; otherwise ep = 0: the logits alone, routed by the
+  // Top-K kernel (a warp per token over every SM), which measured faster
+  if (router_routes_in_epilogue(a.T, a.d, a.E, has_gate)) p.ep = a.E <= 8 ? 8 : 16;
   switch (n) {
     case 16: return launch_mode<RT, 16>(p, s);
     case 32: return launch_mode<RT, 32>(p, s);
@@ -1390,19 +1654,29 @@ cudaError_t launch_router_tc(const RouteArgs &a, cudaStream_t s) {
 
 cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
   const int d = a.d, F = a.F, E = a.n_groups;
+  const bool gather = a.x != nullptr;   // A rows gathered from x through src_of
+  if (gather && !pair_enabled()) return cudaErrorNotSupported;
   void *H = a.H_save ? a.H_save : a.H_tmp;
   TcParams p{};
   p.n_groups = E; p.max_rows = a.max_rows; p.d = d; p.F = F; p.offsets = a.offsets;
   p.status = a.status;
   // GU
-  if (!make_map(&p.tmA, a.Xp, d, a.max_rows, 128)) return cudaErrorInvalidValue;
+  if (!gather && !make_map(&p.tmA, a.Xp, d, a.max_rows, 128)) return cudaErrorInvalidValue;
   if (!make_map(&p.tmB, a.W_gu, d, (uint64_t)E * 2 * F, 128)) return cudaErrorInvalidValue;
   p.mode = GU; p.N = F; p.K_fixed = d; p.b_group_rows = 2 * (int64_t)F;
   p.out0 = H; p.out1 = a.A_save;
   if (!make_store_map(&p.tmO0, H, 2, F, a.max_rows)) return cudaErrorInvalidValue;
   if (a.A_save && !make_store_map(&p.tmO1, a.A_save, 2, 2 * (uint64_t)F, a.max_rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_bn<GU>(p, s);
+  cudaError_t e;
+  if (gather) {
+    // one-row boxes of x: the gather warps load each permuted row by itself
+    if (!make_map(&p.tmX, a.x, d, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
+    p.src_of = a.src_of; p.gK = a.K; p.gT = a.T;
+    e = launch_pair<GU, 128, 1, true>(p, s);
+  } else {
+    e = launch_bn<GU>(p, s);
+  }
   if (e != cudaSuccess) return e;
   // DOWN
   TcParams q = p;

@@ -19,6 +19,14 @@
 namespace moe {
 namespace {
 
+// Programmatic dependent launch: the Top-K and capacity kernels are launched
+// while their predecessor still runs and wait here, before reading anything
+// it wrote, until it has completed and its writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Fused router: one warp per token; the CTA stages a chunk of W_r (and w_sg)
 // in shared memory as fp32 and every warp reuses it for its token.
@@ -102,148 +110,153 @@ router_fused_kernel(RouteArgs a) {
 }
 
 __global__ void __launch_bounds__(256) topk_from_logits_kernel(RouteArgs a) {
+  pdl_wait();   // the logits (or their split partial sums) come from the router GEMM
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= a.T) return;
-  float l0, l1;
-  if (a.rt_split > 1) {
-    // the router GEMM's K-split partial sums, added in split order, then the
-    // bias; the logits (and the gate logit) are written here
-    const int has_gate = a.gate_logit != nullptr ? 1 : 0;
-    const int C = a.E + has_gate;
-    float s0 = 0.0f, s1 = 0.0f, sg = 0.0f;
-    for (int k = 0; k < a.rt_split; ++k) {
-      const float *P = a.rt_part + ((int64_t)k * a.T + t) * C;
-      const float v0 = lane < a.E ? P[lane] : 0.0f;
-      const float v1 = lane + 32 < a.E ? P[lane + 32] : 0.0f;
-      const float vg = (has_gate && lane == 0) ? P[a.E] : 0.0f;
-      s0 = k == 0 ? v0 : __fadd_rn(s0, v0);
-      s1 = k == 0 ? v1 : __fadd_rn(s1, v1);
-      sg = k == 0 ? vg : __fadd_rn(sg, vg);
-    }
-    if (a.b_r != nullptr) {
-      if (lane < a.E) s0 = __fadd_rn(s0, a.b_r[lane]);
-      if (lane + 32 < a.E) s1 = __fadd_rn(s1, a.b_r[lane + 32]);
-    }
-    float *l = a.logits + t * a.E;
-    if (lane < a.E) l[lane] = s0;
-    if (lane + 32 < a.E) l[lane + 32] = s1;
-    if (has_gate && lane == 0) a.gate_logit[t] = sg;
-    l0 = lane < a.E ? s0 : 0.0f;
-    l1 = lane + 32 < a.E ? s1 : 0.0f;
-  } else {
-    const float *l = a.logits + t * a.E;
-    l0 = lane < a.E ? l[lane] : 0.0f;
-    l1 = lane + 32 < a.E ? l[lane + 32] : 0.0f;
-  }
+  const float *l = a.logits + t * a.E;
+  const float l0 = lane < a.E ? l[lane] : 0.0f;
+  const float l1 = lane + 32 < a.E ? l[lane + 32] : 0.0f;
   spec::softmax_topk_warp(l0, l1, a.E, a.K, a.renorm, a.topk_idx + t * a.K, a.topk_prob + t * a.K,
                     a.topk_w + t * a.K, a.keep + t * a.K);
 }
 
 // ---------------------------------------------------------------------------
-// Capacity dropping: one CTA per (sub-sequence j, expert e). Candidates are
-// the assignments (t, k) of the sub-sequence routed to e, keyed by
-// (fp32 bits of p) << 32 | (2^32 - 1 - t): a larger key is a higher
-// probability, then a lower token index. Keys are unique, so the cap largest
-// are found exactly by an MSB radix select (8-bit digits) of the cap-th
-// largest key. The select stops at the first digit whose bin is kept whole:
-// the threshold is then that bin's prefix with zero low bits, which every key
-// of the bin reaches and no key of a lower bin does.
+// Capacity dropping, in two passes over the Top-K slots.
+//   bucket: one thread per slot (t, k) appends the slot's key to the list of
+//     its (sub-sequence j, expert e) in the workspace (warp-aggregated
+//     atomics on the per-list counters, which the call zeroes first);
+//   select: one CTA per (j, e) whose list holds more than cap keys finds the
+//     cap-th largest key and clears keep for the keys below it (the Top-K
+//     step has set every keep to 1).
+// Key of a slot: (fp32 bits of p) << 32 | (2^32 - 1 - (t' * 8 + k)),
+// t' = t - (first token of the sub-sequence): a larger key is a higher
+// probability, then a lower token index (an expert takes at most one slot of
+// a token, so k never decides). Keys are unique, so the cap largest are found
+// exactly by an MSB radix select (8-bit digits) of the cap-th largest key.
+// The select stops at the first digit whose bin is kept whole: the threshold
+// is then that bin's prefix with zero low bits, which every key of the bin
+// reaches and no key of a lower bin does. The order of a list does not
+// matter, so the appends need no ordering.
+constexpr int kBucketThreads = 256;
 constexpr int kCapThreads = 512;
 constexpr int kCapSmemKeys = 16384;   // candidates kept in shared memory (128 KB)
+constexpr int64_t kCapMaxSubseq = int64_t(1) << 29;   // t' * 8 + k fits in 32 bits
+
+__global__ void __launch_bounds__(kBucketThreads)
+capacity_bucket_kernel(RouteArgs a, uint32_t *counts) {
+  pdl_wait();   // topk_idx and topk_prob come from the Top-K step
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // slot t * K + k
+  const int K = a.K, E = a.E;
+  bool valid = false;
+  uint32_t list = 0xFFFFFFFFu;
+  unsigned long long key = 0;
+  if (i < a.T * K) {
+    const int64_t t = i / K;
+    const int k = (int)(i - t * K);
+    const int e = a.topk_idx[i];
+    if (e >= 0 && e < E) {
+      const int64_t j = t / a.S;
+      const uint32_t slot = (uint32_t)((t - j * a.S) * 8 + k);
+      key = ((unsigned long long)__float_as_uint(a.topk_prob[i]) << 32) |
+            (unsigned long long)(0xFFFFFFFFu - slot);
+      list = (uint32_t)(j * E + e);
+      valid = true;
+    } else {
+      report(a.status, MOE_ERR_DEVICE, kInfoExpertRange);
+    }
+  }
+  // one atomic per list and warp: lanes of the same list take consecutive places
+  const uint32_t peers = __match_any_sync(0xffffffffu, list);
+  const int leader = __ffs(peers) - 1;
+  uint32_t base = 0;
+  if (valid && lane == leader) base = atomicAdd(&counts[list], (uint32_t)__popc(peers));
+  base = __shfl_sync(peers, base, leader);
+  if (valid) {
+    const uint32_t pos = base + (uint32_t)__popc(peers & ((1u << lane) - 1u));
+    a.cap_keys[(int64_t)list * a.S + pos] = key;
+  }
+}
 
 __global__ void __launch_bounds__(kCapThreads)
-capacity_kernel(RouteArgs a, int cap_full, int cap_last, int keys_in_smem) {
+capacity_select_kernel(RouteArgs a, const uint32_t *counts, int cap_full, int cap_last,
+                       int keys_in_smem) {
   extern __shared__ unsigned long long skeys[];
-  __shared__ uint32_t n_cand;
   __shared__ uint32_t hist[256];
   __shared__ unsigned long long sh_prefix;
   __shared__ uint32_t sh_need;
   __shared__ int sh_done;
+  pdl_wait();   // the lists come from the bucket pass
   const int j = blockIdx.x, e = blockIdx.y;
   const int64_t lo = (int64_t)j * a.S;
   const int64_t hi = min(a.T, lo + a.S);
   const int cap = (hi - lo == a.S) ? cap_full : cap_last;
-  unsigned long long *keys =
-      keys_in_smem ? skeys : a.cap_keys + ((int64_t)j * a.E + e) * a.S;
-  const int K = a.K;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) n_cand = 0;
-  __syncthreads();
-  // candidates: one shared-memory atomic per warp and slot
-  const uint32_t lanes_below = (1u << lane) - 1u;
-  for (int64_t t0 = lo; t0 < hi; t0 += blockDim.x) {
-    const int64_t t = t0 + threadIdx.x;
-    for (int k = 0; k < K; ++k) {
-      const bool m = t < hi && a.topk_idx[t * K + k] == e;
-      const uint32_t ballot = __ballot_sync(0xffffffffu, m);
-      if (ballot == 0u) continue;
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(&n_cand, (uint32_t)__popc(ballot));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (m) {
-        const uint32_t pbits = __float_as_uint(a.topk_prob[t * K + k]);
-        keys[base + __popc(ballot & lanes_below)] =
-            ((unsigned long long)pbits << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)t);
-      }
-    }
+  const int64_t list = (int64_t)j * a.E + e;
+  const uint32_t n = counts[list];
+  if (n <= (uint32_t)cap) return;   // every assignment of the list is kept
+  const unsigned long long *gkeys = a.cap_keys + list * a.S;
+  const unsigned long long *keys = gkeys;
+  if (keys_in_smem) {
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) skeys[i] = gkeys[i];
+    keys = skeys;
   }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) { sh_prefix = 0; sh_need = (uint32_t)cap; sh_done = 0; }
   __syncthreads();
-  const uint32_t n = n_cand;
-  unsigned long long threshold = 0;
-  if (n > (uint32_t)cap) {
-    if (threadIdx.x == 0) { sh_prefix = 0; sh_need = (uint32_t)cap; sh_done = 0; }
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
-      __syncthreads();
-      const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
-      const unsigned long long pre = sh_prefix;
-      for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
-        const unsigned long long key = keys[i];
-        if ((key & hmask) == (pre & hmask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0;
+    __syncthreads();
+    const unsigned long long hmask = (shift == 56) ? 0ull : (~0ull << (shift + 8));
+    const unsigned long long pre = sh_prefix;
+    for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
+      const unsigned long long key = keys[i];
+      if ((key & hmask) == (pre & hmask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // digit holding the need-th largest key: lane l owns bins 255-8l down
+      // to 248-8l; an inclusive scan over lanes counts the keys above
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * lane - i];
+        sum += c[i];
       }
-      __syncthreads();
-      if (warp == 0) {
-        // digit holding the need-th largest key: lane l owns bins 255-8l down
-        // to 248-8l; an inclusive scan over lanes counts the keys above
-        uint32_t c[8], sum = 0;
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - sum;
+      const uint32_t need = sh_need;
+      const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
+      if (lane == __ffs(hit) - 1) {
+        uint32_t cum = excl, cnt = 0;
+        int digit = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          c[i] = hist[255 - 8 * lane - i];
-          sum += c[i];
+          if (cum + c[i] >= need) { digit = 255 - 8 * lane - i; cnt = c[i]; break; }
+          cum += c[i];
         }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - sum;
-        const uint32_t need = sh_need;
-        const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-        if (lane == __ffs(hit) - 1) {
-          uint32_t cum = excl, cnt = 0;
-          int digit = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (cum + c[i] >= need) { digit = 255 - 8 * lane - i; cnt = c[i]; break; }
-            cum += c[i];
-          }
-          sh_need = need - cum;
-          sh_prefix = pre | ((unsigned long long)digit << shift);
-          sh_done = (need - cum == cnt) ? 1 : 0;   // the digit's whole bin is kept
-        }
+        sh_need = need - cum;
+        sh_prefix = pre | ((unsigned long long)digit << shift);
+        sh_done = (need - cum == cnt) ? 1 : 0;   // the digit's whole bin is kept
       }
-      __syncthreads();
-      if (sh_done) break;
     }
-    threshold = sh_prefix;
+    __syncthreads();
+    if (sh_done) break;
   }
+  const unsigned long long threshold = sh_prefix;
+  const int K = a.K;
   for (uint32_t i = threadIdx.x; i < n; i += blockDim.x) {
     const unsigned long long key = keys[i];
-    const int64_t t = (int64_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-    for (int k = 0; k < K; ++k) {
-      if (a.topk_idx[t * K + k] == e) a.keep[t * K + k] = key >= threshold ? 1 : 0;
+    if (key < threshold) {
+      const uint32_t slot = 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+      a.keep[(lo + (slot >> 3)) * K + (slot & 7u)] = 0;
     }
   }
 }
@@ -274,10 +287,26 @@ cudaError_t launch_router_fused(const RouteArgs &a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Launch with programmatic stream serialization (the kernels call
+// griddepcontrol.wait before reading their predecessor's outputs).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 cudaError_t launch_topk_from_logits(const RouteArgs &a, cudaStream_t s) {
   const unsigned grid = (unsigned)((a.T * 32 + 255) / 256);
-  topk_from_logits_kernel<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(topk_from_logits_kernel, dim3(grid), dim3(256), 0, s, a);
 }
 
 int64_t padded_rows_per_expert(int64_t T, int64_t S, int K, int E, float cf) {
@@ -291,18 +320,25 @@ int64_t padded_rows_per_expert(int64_t T, int64_t S, int K, int E, float cf) {
 }
 
 cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s) {
+  if (a.S >= kCapMaxSubseq || a.K < 1 || a.K > 8 || a.cap_counts == nullptr)
+    return cudaErrorInvalidValue;
   const int64_t n_sub = (a.T + a.S - 1) / a.S;
   const int64_t last = a.T - (n_sub - 1) * a.S;
   const int cap_full = capacity_of(a.cf, a.S, a.K, a.E);
   const int cap_last = capacity_of(a.cf, last, a.K, a.E);
-  dim3 grid((unsigned)n_sub, (unsigned)a.E);
+  const int64_t slots = a.T * a.K;
+  cudaError_t e = launch_pdl(capacity_bucket_kernel,
+                             dim3((unsigned)((slots + kBucketThreads - 1) / kBucketThreads)),
+                             dim3(kBucketThreads), 0, s, a, a.cap_counts);
+  if (e != cudaSuccess) return e;
   const int in_smem = a.S <= kCapSmemKeys ? 1 : 0;
   const size_t smem = in_smem ? (size_t)a.S * sizeof(unsigned long long) : 0;
-  cudaError_t e = cudaFuncSetAttribute(capacity_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  e = cudaFuncSetAttribute(capacity_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
   if (e != cudaSuccess) return e;
-  capacity_kernel<<<grid, kCapThreads, smem, s>>>(a, cap_full, cap_last, in_smem);
-  return cudaGetLastError();
+  return launch_pdl(capacity_select_kernel, dim3((unsigned)n_sub, (unsigned)a.E),
+                    dim3(kCapThreads), smem, s, a, (const uint32_t *)a.cap_counts, cap_full,
+                    cap_last, in_smem);
 }
 
 }  // namespace moe

@@ -36,13 +36,22 @@ class MoELayer:
 
     layout="padded" (token dropping only) uses the fixed GShard-style layout of
     moe_permute_padded: expert e owns rows [e*C, (e+1)*C), zero rows after its
-    kept ones, and the grouped GEMMs run every padded row."""
+    kept ones, and the grouped GEMMs run every padded row.
+
+    gather=True (bf16, forward only, etp = 1) fuses the permutation into the
+    routed experts' gate/up GEMM: moe_permute builds the map alone (Xp NULL)
+    and moe_expert_ffn_gather reads each permuted row from x through src_of,
+    so the permuted copy of the tokens is never written."""
 
     def __init__(self, cfg, weights: dict, device="cuda", backward=None, etp: int = 1,
-                 layout: str = "compact"):
+                 layout: str = "compact", gather: bool = False):
         self.cfg = cfg
         self.etp = etp
         self.layout = layout
+        self.gather = gather
+        if gather and (etp != 1 or cfg.dtype != "bf16"
+                       or (cfg.backward if backward is None else backward)):
+            raise ValueError("gather=True serves the bf16 forward-only layer with etp = 1")
         self.shape = L.shape_of(cfg)
         self.backward_enabled = cfg.backward if backward is None else backward
         self.w = weights
@@ -67,7 +76,7 @@ class MoELayer:
         self.topk_prob = z(T, K, dtype=torch.float32)
         self.topk_w = z(T, K, dtype=torch.float32)
         self.keep = z(T, K, dtype=torch.uint8)
-        self.Xp = z(N, d)
+        self.Xp = None if gather else z(N, d)
         self.row_of = z(T, K, dtype=torch.int32)
         self.src_of = z(N, dtype=torch.int32)
         self.counts = z(E, dtype=torch.int32)
@@ -146,6 +155,11 @@ class MoELayer:
 
     def routed_ffn(self, stream=None):
         c, w = self.cfg, self.w
+        if self.gather:
+            L.moe_expert_ffn_gather(self.rows, c.d, c.F, c.E, self.offsets, self.x, c.T, c.K,
+                                    self.src_of, w["W_gu"], w["W_down"], self.A_save, self.H,
+                                    self.Yp, self.ws, stream)
+            return
         if self.etp == 1:
             L.moe_expert_ffn(self.dtype_code, self.rows, c.d, c.F, c.E, self.offsets, self.Xp,
                              w["W_gu"], w["W_down"], self.A_save, self.H, self.Yp, self.ws, stream)
