@@ -144,40 +144,62 @@ constexpr int kCapThreads = 512;
 constexpr int kCapSmemKeys = 16384;   // candidates kept in shared memory (128 KB)
 constexpr int64_t kCapMaxSubseq = int64_t(1) << 29;   // t' * 8 + k fits in 32 bits
 
+// A bucket CTA takes the slots of `tpc` consecutive tokens (tpc <= S, so at
+// most two sub-sequences), kBucketRounds per thread, coalesced. It counts its
+// keys per list in shared memory (a place inside its share of each list),
+// reserves its share of each list with one global atomic, then writes. Two
+// rounds (512 slots per CTA) keep the grid at 64 CTAs or more on the
+// Mixtral-8x22B shape (16384 slots).
+constexpr int kBucketRounds = 2;
+
 __global__ void __launch_bounds__(kBucketThreads)
-capacity_bucket_kernel(RouteArgs a, uint32_t *counts) {
+capacity_bucket_kernel(RouteArgs a, uint32_t *counts, int tpc) {
+  __shared__ uint32_t lcnt[2][64], lbase[2][64];
   pdl_wait();   // topk_idx and topk_prob come from the Top-K step
   pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // slot t * K + k
   const int K = a.K, E = a.E;
-  bool valid = false;
-  uint32_t list = 0xFFFFFFFFu;
-  unsigned long long key = 0;
-  if (i < a.T * K) {
-    const int64_t t = i / K;
-    const int k = (int)(i - t * K);
-    const int e = a.topk_idx[i];
-    if (e >= 0 && e < E) {
-      const int64_t j = t / a.S;
-      const uint32_t slot = (uint32_t)((t - j * a.S) * 8 + k);
-      key = ((unsigned long long)__float_as_uint(a.topk_prob[i]) << 32) |
-            (unsigned long long)(0xFFFFFFFFu - slot);
-      list = (uint32_t)(j * E + e);
-      valid = true;
-    } else {
-      report(a.status, MOE_ERR_DEVICE, kInfoExpertRange);
+  const int64_t t0 = (int64_t)blockIdx.x * tpc;
+  const int64_t s0 = t0 * K, s1 = min(a.T, t0 + tpc) * K;   // this CTA's slots
+  const int64_t j0 = t0 / a.S;
+  for (int i = threadIdx.x; i < 2 * 64; i += blockDim.x) (&lcnt[0][0])[i] = 0;
+  __syncthreads();
+  int sel[kBucketRounds];           // list within the CTA (jj * 64 + e), -1 if none
+  uint32_t pos[kBucketRounds];      // place within the CTA's share of that list
+  unsigned long long key[kBucketRounds];
+#pragma unroll
+  for (int r = 0; r < kBucketRounds; ++r) {
+    const int64_t i = s0 + (int64_t)r * blockDim.x + threadIdx.x;
+    sel[r] = -1;
+    pos[r] = 0;
+    key[r] = 0;
+    if (i < s1) {
+      const int64_t t = i / K;
+      const int k = (int)(i - t * K);
+      const int e = a.topk_idx[i];
+      if (e >= 0 && e < E) {
+        const int64_t j = t / a.S;
+        const uint32_t slot = (uint32_t)((t - j * a.S) * 8 + k);
+        key[r] = ((unsigned long long)__float_as_uint(a.topk_prob[i]) << 32) |
+                 (unsigned long long)(0xFFFFFFFFu - slot);
+        sel[r] = (int)(j - j0) * 64 + e;
+        pos[r] = atomicAdd(&(&lcnt[0][0])[sel[r]], 1u);
+      } else {
+        report(a.status, MOE_ERR_DEVICE, kInfoExpertRange);
+      }
     }
   }
-  // one atomic per list and warp: lanes of the same list take consecutive places
-  const uint32_t peers = __match_any_sync(0xffffffffu, list);
-  const int leader = __ffs(peers) - 1;
-  uint32_t base = 0;
-  if (valid && lane == leader) base = atomicAdd(&counts[list], (uint32_t)__popc(peers));
-  base = __shfl_sync(peers, base, leader);
-  if (valid) {
-    const uint32_t pos = base + (uint32_t)__popc(peers & ((1u << lane) - 1u));
-    a.cap_keys[(int64_t)list * a.S + pos] = key;
+  __syncthreads();
+  for (int l = threadIdx.x; l < 2 * 64; l += blockDim.x) {
+    const uint32_t c = (&lcnt[0][0])[l];
+    if (c > 0) (&lbase[0][0])[l] = atomicAdd(&counts[(j0 + l / 64) * E + (l % 64)], c);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kBucketRounds; ++r) {
+    if (sel[r] >= 0) {
+      const int64_t list = (j0 + sel[r] / 64) * E + (sel[r] % 64);
+      a.cap_keys[list * a.S + (&lbase[0][0])[sel[r]] + pos[r]] = key[r];
+    }
   }
 }
 
@@ -326,10 +348,12 @@ cudaError_t launch_capacity(const RouteArgs &a, cudaStream_t s) {
   const int64_t last = a.T - (n_sub - 1) * a.S;
   const int cap_full = capacity_of(a.cf, a.S, a.K, a.E);
   const int cap_last = capacity_of(a.cf, last, a.K, a.E);
-  const int64_t slots = a.T * a.K;
-  cudaError_t e = launch_pdl(capacity_bucket_kernel,
-                             dim3((unsigned)((slots + kBucketThreads - 1) / kBucketThreads)),
-                             dim3(kBucketThreads), 0, s, a, a.cap_counts);
+  // tokens per bucket CTA: its slots fill kBucketRounds rounds of the block,
+  // and no more than one sub-sequence's worth (so at most two sub-sequences)
+  int64_t tpc = kBucketRounds * kBucketThreads / a.K;
+  if (tpc > a.S) tpc = a.S;
+  cudaError_t e = launch_pdl(capacity_bucket_kernel, dim3((unsigned)((a.T + tpc - 1) / tpc)),
+                             dim3(kBucketThreads), 0, s, a, a.cap_counts, (int)tpc);
   if (e != cudaSuccess) return e;
   const int in_smem = a.S <= kCapSmemKeys ? 1 : 0;
   const size_t smem = in_smem ? (size_t)a.S * sizeof(unsigned long long) : 0;

@@ -42,13 +42,23 @@ __device__ __forceinline__ float exp_spec(float u) {
   return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
+// fp32 value <-> unsigned key with the same order (negative values flipped),
+// for warp-wide maxima with one redux instruction; exact both ways
+__device__ __forceinline__ unsigned ordered_key(float v) {
+  const unsigned b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ordered_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // p for the two experts a lane holds (lane, lane+32); -1 for absent experts.
 __device__ __forceinline__ void softmax_warp(float l0, float l1, int E, float &p0, float &p1) {
   const int lane = threadIdx.x & 31;
   const bool v0 = lane < E, v1 = lane + 32 < E;
-  float m = fmaxf(v0 ? l0 : -INFINITY, v1 ? l1 : -INFINITY);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  // the maximum is exact in any order: one warp-wide redux of ordered keys
+  const float m = ordered_value(__reduce_max_sync(
+      0xffffffffu, ordered_key(fmaxf(v0 ? l0 : -INFINITY, v1 ? l1 : -INFINITY))));
   const float q0 = v0 ? exp_spec(__fsub_rn(l0, m)) : 0.0f;
   const float q1 = v1 ? exp_spec(__fsub_rn(l1, m)) : 0.0f;
   float s = __fadd_rn(q0, q1);
@@ -69,16 +79,14 @@ __device__ __forceinline__ void softmax_topk_warp(float l0, float l1, int E, int
   float my_prob = 0.0f;
   int my_idx = 0;
   for (int k = 0; k < K; ++k) {
-    // lane-local best (lower index wins ties: expert `lane` before lane+32)
-    float bp = p0;
-    int bi = lane;
-    if (p1 > bp) { bp = p1; bi = lane + 32; }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (op > bp || (op == bp && oi < bi)) { bp = op; bi = oi; }
-    }
+    // lane-local best (lower index wins ties: expert `lane` before lane+32),
+    // then the warp's largest p and the lowest expert index holding it
+    float lp = p0;
+    int li = lane;
+    if (p1 > lp) { lp = p1; li = lane + 32; }
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, ordered_key(lp));
+    const int bi = (int)__reduce_min_sync(0xffffffffu, ordered_key(lp) == kmax ? (unsigned)li : 64u);
+    const float bp = ordered_value(kmax);
     if (bi == lane) p0 = -2.0f;
     if (bi == lane + 32) p1 = -2.0f;
     if (lane == k) { my_prob = bp; my_idx = bi; }
