@@ -271,28 +271,53 @@ def route_algorithmic_bytes(cfg) -> int:
     return n + cfg.T * cfg.K * (4 + 4 + 4 + 1)
 
 
-def launches_per_step(cfg, etp: int = 1) -> int:
+def launches_per_step(cfg, etp: int = 1, gather: bool = False) -> int:
+    """Kernels of this library launched per step (bf16 row-grouped GEMMs are a
+    CTA-pair launch plus the single-CTA launch for half-empty last tiles)."""
     bf16 = cfg.dtype == "bf16"
-    n = 2 if bf16 else 1                   # router: logits GEMM + Top-K (fp32: one fused kernel)
-    n += 1 if cfg.drop else 0             # capacity
-    n += 3                                 # map count, map scatter, row copy
-    n += 2 * etp + (1 if etp > 1 else 0)   # routed grouped GEMMs per F-shard [+ partial sum]
-    n += 2 if cfg.Fs else 0                # shared expert
+    tc = bf16 and cfg.d % 64 == 0
+    n = 1 if tc and (cfg.E > 16 or router_splits(cfg) > 1) else 0   # Top-K kernel after the router GEMM
+    n += 1                                 # router GEMM (fp32: the fused router kernel)
+    n += 2 if cfg.drop else 0              # capacity: bucket + select
+    n += 3 if not gather else 2            # map count, map scatter, row copy (fused: no copy)
+    fwd_gemm = (4 if bf16 else 2)          # gate/up and down, each pair + tails
+    if gather:
+        fwd_gemm = 3                       # gathered gate/up (no tails) + down + tails
+    n += fwd_gemm * etp + (1 if etp > 1 else 0)   # routed experts per F-shard [+ partial sum]
+    n += (4 if bf16 else 2) if cfg.Fs else 0      # shared expert
     n += 1                                 # un-permute
     if cfg.backward:
         gm = 2 if bf16 else 0              # group tensor maps of the two weight-gradient GEMMs
+        # dH and dXp with their tail launches, dW_down, dW_gu
+        bwd_gemm = (6 if bf16 else 4) + gm
         n += 1                             # un-permute backward
-        n += (4 + gm) * etp + (1 if etp > 1 else 0)   # dH, dX, dW_down, dW_gu per shard [+ dXp sum]
-        n += (4 + gm) if cfg.Fs else 0
+        n += bwd_gemm * etp + (1 if etp > 1 else 0)
+        n += bwd_gemm if cfg.Fs else 0
         if bf16 and cfg.d % 256 == 0:      # router backward on the tensor cores:
-            # dl, dl planes, [W_r planes + dx GEMM | dx kernel with the shared-expert addend],
-            # group maps, dW_r GEMM, plane sum
-            n += 6 + (0 if cfg.Fs else 1)
+            # dl, dl planes, [W_r planes + dx GEMM (+ tails) | dx kernel with the
+            # shared-expert addend], group maps, dW_r GEMM, plane sum
+            n += 6 + (0 if cfg.Fs else 2)
         else:
             n += 4                         # dl, dx, dW_r partials, reduce
         n += 1 if cfg.bias else 0          # db_r
         n += 1                             # permute backward
     return n
+
+
+def router_splits(cfg) -> int:
+    """K parts of the tensor-core router GEMM (as libmoe.so chooses them: as
+    many as leave no SM idle on a 152-SM GB300, at most 4, >= 8 K blocks each,
+    and at most what the even CTA's exchange buffer holds)."""
+    mtiles = (cfg.T + 127) // 128
+    kb = cfg.d // 64
+    s = max(1, min(4, 152 // mtiles if mtiles else 1, kb // 8))
+    per = (kb + s - 1) // s
+    s = (kb + per - 1) // per
+    gate = 1 if cfg.Fs else 0
+    n = (cfg.E + 15) // 16 * 16 + 16 * gate
+    stage = 16384 + (n * 128 + 1023) // 1024 * 1024
+    room = 4 * 49152 + 32768 - 6 * stage
+    return min(s, 1 + room // (128 * (cfg.E + gate) * 4))
 
 
 def run_reference(args, cfg, rank, world):
@@ -624,9 +649,8 @@ def main():
             "clocks": clk,
             "e2e": {"value": e2e["value"], "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (launches_per_step(cfg, args.etp)
-                             + (1 if args.layout == "padded" else 0)
-                             - (1 if args.gather else 0)) * args.steps,
+            "gpu_launches": (launches_per_step(cfg, args.etp, args.gather)
+                             + (1 if args.layout == "padded" else 0)) * args.steps,
             "roofline": {"kernel": ("routed experts' grouped GEMMs, forward + backward (moe_expert_ffn: "
                                     "gate/up + down; moe_expert_ffn_bwd: dH, dXp, dW_down, dW_gu)"
                                     if cfg.backward else

@@ -52,14 +52,28 @@ def test_aggregate_single_rank():
 def test_launch_counts():
     import bench
     from synthetic import get_config
-    assert bench.launches_per_step(get_config("mixtral_8x22b")) == 9
-    # llama: fwd 8; bwd: un-permute 1, FFN 4 + 2 maps, router 7, permute 1
-    assert bench.launches_per_step(get_config("llama3_8x70b")) == 8 + 15
-    # qwen: fwd 10; bwd: 1 + (6 + 6) + router 6 + db 1 + permute 1
-    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 10 + 21
-    # g8t8: fwd 9; bwd 1 + 6 + 7 + 1
-    assert bench.launches_per_step(get_config("mixtral_8x22b_g8t8")) == 9 + 15
+    # mixtral fwd: router GEMM + Top-K (K split in two), bucket + select, map count,
+    # scatter, row copy, gate/up and down (pair + tail launch each), un-permute
+    assert bench.launches_per_step(get_config("mixtral_8x22b")) == 12
+    assert bench.launches_per_step(get_config("mixtral_8x22b"), gather=True) == 10
+    # llama: fwd 9 (routing in the router GEMM's epilogue); bwd: un-permute 1,
+    # FFN 6 + 2 maps, router 8 (dl, planes, W_r planes, dx pair + tail, maps,
+    # dW_r, plane sum), permute 1
+    assert bench.launches_per_step(get_config("llama3_8x70b")) == 9 + 18
+    # qwen: fwd 14 (shared expert 4); bwd: 1 + (8 + 8) + router 6 + db 1 + permute 1
+    assert bench.launches_per_step(get_config("qwen2_57b_a14b")) == 14 + 25
+    # g8t8: fwd 12; bwd 1 + 8 + 8 + 1
+    assert bench.launches_per_step(get_config("mixtral_8x22b_g8t8")) == 12 + 18
     assert bench.launches_per_step(get_config("tiny_f32")) == 7
+
+
+def test_router_split_matches_the_library():
+    """bench.router_splits restates libmoe.so's choice of K parts (it sizes the
+    launch count); the library's router_k_split is exercised on the GPU."""
+    import bench
+    from synthetic import get_config
+    assert [bench.router_splits(get_config(n)) for n in
+            ("mixtral_8x22b", "qwen2_57b_a14b", "mixtral_8x22b_g8t8", "llama3_8x70b")] == [2, 2, 1, 1]
 
 
 def test_traffic_key_ignores_comments_only(tmp_path):

@@ -100,6 +100,14 @@ struct TcParams {
   // zero-fills the K rows past the group's end of a ragged last K block
   const CUtensorMap *gmaps;
   int fault_stall;   // test hook: the producer issues no loads (waits run out)
+  // row-grouped modes, ragged tails: a group whose last 256 rows hold at most
+  // 128 rows (0 < rows % 256 <= 128) has that tail computed by the single-CTA
+  // kernel (128-row tiles) instead of a half-empty CTA-pair tile.
+  //   1: the pair kernel leaves such tails out (and lets the tail kernel launch
+  //      as its programmatic dependent);
+  //   2: the single-CTA kernel computes only those tails (and waits for the
+  //      pair kernel before it completes, so later work sees both)
+  int tail_mode;
   // GU with a gathered A operand (the permutation fused into the GEMM): row
   // R < offsets[n_groups] of the tile is token src_of[R] / gK of x [gT, d]
   // (through tmX); other rows, and rows with src_of < 0 (padding), are zero
@@ -389,6 +397,7 @@ struct SharedState {
   int total_tiles;
   int tile_start[65];  // ROWS mode: first tile index of each group
   int mtiles[64];      // ROWS mode: m-tiles of each group
+  int mbase[64];       // ROWS mode: first m-tile of each group's tile range
 };
 
 struct Tile {
@@ -417,11 +426,18 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, const SharedState
     const int mt = st.mtiles[g];
     t.g = g;
     t.n = loc / mt;
-    t.m = loc % mt;
+    t.m = st.mbase[g] + loc % mt;
     t.row0 = p.offsets[g];
     t.rows = p.offsets[g + 1] - t.row0;
   }
   return t;
+}
+
+// 0 < rows % 256 <= 128: the group's last 256 rows would fill at most half a
+// CTA-pair tile
+__device__ __forceinline__ bool half_tail(int rows) {
+  const int rem = rows % 256;
+  return rows > 0 && rem > 0 && rem <= 128;
 }
 
 __device__ bool wait_bounded(SharedState &st, uint32_t bar, uint32_t parity, uint32_t *status,
@@ -846,7 +862,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int g = 0; g < p.n_groups; ++g) {
         const int rows = p.offsets[g + 1] - p.offsets[g];
         if (rows < 0) bad = true;
-        const int mt = rows > 0 ? (rows + BM - 1) / BM : 0;
+        int mt = rows > 0 ? (rows + BM - 1) / BM : 0;
+        st.mbase[g] = 0;
+        if (p.tail_mode == 2) {   // only the half-tile tail: the 128 rows after the full pairs
+          mt = half_tail(rows) ? 1 : 0;
+          st.mbase[g] = rows > 0 ? (rows / 256) * 2 : 0;
+        }
         st.tile_start[g] = total;
         st.mtiles[g] = mt > 0 ? mt : 1;
         total += mt * NT;
@@ -1040,6 +1061,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                  "r"(kTmemCols)
                  : "memory");
   }
+  // tail kernel: complete only after the pair kernel it followed, so that
+  // whatever the stream runs next sees the rows of both
+  if (p.tail_mode == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 
@@ -1102,6 +1126,9 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
   constexpr uint32_t kTx = 2u * kOwnTx;
   constexpr uint32_t kIdesc = instr_desc(256, MMA_N, TR::a_mn, TR::b_mn);
 
+  // the tail kernel (single-CTA, half-empty last tiles) may launch now: its
+  // CTAs take SMs as this grid's CTAs leave
+  if (p.tail_mode == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -1125,9 +1152,11 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
       for (int g = 0; g < p.n_groups; ++g) {
         const int rows = p.offsets[g + 1] - p.offsets[g];
         if (rows < 0) bad = true;
-        const int mt = rows > 0 ? (rows + 255) / 256 : 0;   // 256-row pair tiles
+        int mt = rows > 0 ? (rows + 255) / 256 : 0;   // 256-row pair tiles
+        if (p.tail_mode == 1 && half_tail(rows)) --mt;  // the tail kernel takes it
         st.tile_start[g] = total;
         st.mtiles[g] = mt > 0 ? mt : 1;
+        st.mbase[g] = 0;
         total += mt * NT;
       }
       st.tile_start[p.n_groups] = total;
@@ -1526,6 +1555,19 @@ cudaError_t launch_mode(TcParams p, cudaStream_t s) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, p);
   }
+  if (p.tail_mode == 2) {   // programmatic dependent of the pair kernel before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+  }
   k<<<num_sms(), kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
 }
@@ -1569,6 +1611,21 @@ bool pair_enabled() {
 constexpr bool pair_enabled() { return true; }
 #endif
 
+// Pair kernel, then (row-grouped modes) the single-CTA kernel for the groups'
+// half-empty last tiles. The two write disjoint rows. The B tensor maps of the
+// two kernels agree (128-row boxes for K-major B, 64 x 64 boxes for MN-major
+// B) except for the down projection at BN = 128, which keeps its tails.
+template <int MODE, int BN, int NSUB = 1>
+cudaError_t launch_pair_and_tails(TcParams p, cudaStream_t s) {
+  constexpr bool tails = MODE == GU || MODE == DH || MODE == DX || (MODE == DOWN && BN == 256);
+  if constexpr (!tails) return launch_pair<MODE, BN, NSUB>(p, s);
+  p.tail_mode = 1;
+  cudaError_t e = launch_pair<MODE, BN, NSUB>(p, s);
+  if (e != cudaSuccess) return e;
+  p.tail_mode = 2;
+  return launch_mode<MODE, BN>(p, s);
+}
+
 template <int MODE>
 cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
   const bool bn256 = !(MODE == GU || p.N % 256 != 0);
@@ -1582,11 +1639,12 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
       // backward): on the Llama3-8x70B training step that measured 1.1 %
       // faster than two tiles
       if constexpr (MODE == DOWN || MODE == DX)
-        if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192) return launch_pair<MODE, 256, 2>(p, s);
+        if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192)
+          return launch_pair_and_tails<MODE, 256, 2>(p, s);
       if constexpr (red)   // K = a group's rows: the same test on the mean rows per group
         if (bn256 && (p.N / 256) % 2 == 0 && p.max_rows / p.n_groups >= 8192)
           return launch_pair<MODE, 256, 2>(p, s);
-      return bn256 ? launch_pair<MODE, 256>(p, s) : launch_pair<MODE, 128>(p, s);
+      return bn256 ? launch_pair_and_tails<MODE, 256>(p, s) : launch_pair_and_tails<MODE, 128>(p, s);
     }
   }
   return bn256 ? launch_mode<MODE, 256>(p, s) : launch_mode<MODE, 128>(p, s);
