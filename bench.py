@@ -406,7 +406,15 @@ def main():
     if args.override:
         import dataclasses
         kv = dict(item.split("=", 1) for item in args.override.split(","))
-        typed = {k: type(getattr(cfg, k))(v) for k, v in kv.items()}
+
+        def cast(k, v):
+            t = type(getattr(cfg, k))
+            if t is bool:   # bool("False") is True: read the word
+                if v.lower() not in ("0", "1", "false", "true"):
+                    raise ValueError(f"{k}={v}: expected true/false")
+                return v.lower() in ("1", "true")
+            return t(v)
+        typed = {k: cast(k, v) for k, v in kv.items()}
         cfg = dataclasses.replace(cfg, name=f"{cfg.name}[{args.override}]", **typed)
     rank, world, local = dist_env()
     dist = None

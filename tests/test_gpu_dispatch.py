@@ -133,3 +133,46 @@ def test_identity_experts_round_trip():
     o, n = _check_permute(L, cfg, inp["x"], r["topk_idx"], r["keep"])
     got = _unpermute_gpu(L, cfg, o["Xp"], host(o["row_of"]), np.ones((cfg.T, cfg.K), np.float32))
     assert np.array_equal(got, cfg.K * O.decode(inp["x"]))
+
+
+@pytest.mark.parametrize("K", [1, 3, 4, 5, 8])
+@pytest.mark.parametrize("shared", [False, True])
+def test_unpermute_and_backward_every_slot_bound(K, shared):
+    """The un-permute kernels are compiled for slot bounds 1, 2, 4 and 8 (the
+    smallest at or above K): every bound, K below its bound (3, 5), dropped
+    slots and the shared expert, forward and backward, against the oracle."""
+    L = lib()
+    base = get_config("mixtral_8x22b@small")
+    cfg = dataclasses.replace(base, T=333, d=512, E=8, K=K, Fs=256 if shared else 0)
+    rng = np.random.default_rng(10 + K)
+    row_of = np.full((cfg.T, K), -1, np.int32)
+    kept = rng.random((cfg.T, K)) < 0.85
+    row_of[kept] = rng.permutation(int(kept.sum())).astype(np.int32)
+    n = int(kept.sum())
+    Yp = O.round_bf16(rng.standard_normal((n, cfg.d)))
+    w = rng.random((cfg.T, K)).astype(np.float32)
+    dout = O.round_bf16(rng.standard_normal((cfg.T, cfg.d)))
+    Ys = O.round_bf16(rng.standard_normal((cfg.T, cfg.d))) if shared else None
+    z = rng.standard_normal(cfg.T).astype(np.float32) if shared else None
+    s = L.shape_of(cfg)
+    bf = torch.bfloat16
+    Yp_d = torch.as_tensor(Yp, dtype=bf).cuda()
+    Ys_d = torch.as_tensor(Ys, dtype=bf).cuda() if shared else None
+    z_d = torch.as_tensor(z).cuda() if shared else None
+    out = empty((cfg.T, cfg.d), bf)
+    L.moe_unpermute(s, Yp_d, dev(row_of), dev(w), Ys_d, z_d, out)
+    ref = O.unpermute(Yp, row_of, w, Ys, z)
+    assert_close("out", host(out), ref, "bf16")
+    dYp = empty((max(n, 1), cfg.d), bf)
+    dw = empty((cfg.T, K), torch.float32)
+    dYs = empty((cfg.T, cfg.d), bf) if shared else None
+    dz = empty((cfg.T,), torch.float32) if shared else None
+    L.moe_unpermute_bwd(s, torch.as_tensor(dout, dtype=bf).cuda(), Yp_d, dev(row_of), dev(w),
+                        Ys_d, z_d, dYp, dw, dYs, dz)
+    ub = O.unpermute_bwd(O.round_bf16(dout), Yp, row_of, w, Ys, z)
+    # the oracle's dout argument is bf16 bits or values: it decodes arrays of values as is
+    assert_close("dYp", host(dYp)[:n], ub["dYp"], "bf16")
+    assert_close("dw", host(dw), ub["dw"], "bf16")
+    if shared:
+        assert_close("dYs", host(dYs), ub["dYs"], "bf16")
+        assert_close("dz", host(dz), ub["dz"], "bf16")
