@@ -536,6 +536,15 @@ __device__ __forceinline__ void route_row(const TcParams &p, const float (&v)[NV
     }
 }
 
+// Logistic sigmoid 1 / (1 + e^-x) of the SwiGLU epilogues, with the fast
+// division intrinsic (within 2 ulp of fp32 for a divisor in [1, 2^126];
+// 1 + e^-x >= 1, and an overflowed e^-x gives 0). Its results are rounded to
+// bf16 (H, dA), whose unit is 2^16 fp32 ulps; the correctly rounded
+// reciprocal cost the dH epilogue two thirds of its time.
+__device__ __forceinline__ float sigmoid_fast(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+
 // One tile's epilogue for the epilogue warp that owns TMEM lane quarter q.
 // xbuf (router mode with a split K loop, even CTA): the other parts' partial
 // sums, [part - 1][128 rows][E + has_gate].
@@ -636,7 +645,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
             pack_bf16(u, wu, hh * 16);
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h[i] = g[i] * __frcp_rn(1.0f + __expf(-g[i])) * u[i];
+          for (int i = 0; i < 32; ++i) h[i] = g[i] * sigmoid_fast(g[i]) * u[i];
           pack_bf16(h, wh, hh * 16);
         }
         uint8_t *b = stage_begin(sg, lane);
@@ -711,7 +720,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
             load16<__nv_bfloat16>(reinterpret_cast<const __nv_bfloat16 *>(ru + off), U);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float sgm = __frcp_rn(1.0f + __expf(-G[j]));
+              const float sgm = sigmoid_fast(G[j]);
               const float dhv = dh[8 * cc + j];
               dG[j] = dhv * U[j] * sgm * (1.0f + G[j] * (1.0f - sgm));
               dU[j] = dhv * G[j] * sgm;
@@ -749,7 +758,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
         if (valid) {
           float h[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) h[i] = g[i] / (1.0f + __expf(-g[i])) * u[i];
+          for (int i = 0; i < 32; ++i) h[i] = g[i] * sigmoid_fast(g[i]) * u[i];
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             store16<__nv_bfloat16>(H + c * 32 + i, *reinterpret_cast<float(*)[8]>(h + i));
@@ -792,7 +801,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
             load16<__nv_bfloat16>(As + p.F + c * 32 + i, U);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float sg = __frcp_rn(1.0f + __expf(-G[j]));
+              const float sg = sigmoid_fast(G[j]);
               dG[j] = dh[i + j] * U[j] * sg * (1.0f + G[j] * (1.0f - sg));
               dU[j] = dh[i + j] * G[j] * sg;
             }
