@@ -1643,15 +1643,17 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
     if (pair_enabled() && (!red || p.M_fixed % 256 == 0)) {
       // two N tiles per pair tile where the epilogue (no longer overlapped
       // with the next tile's mainloop) is short against a long K loop: the
-      // down projection, dXp and gate/up with K >= 8192 (128 K blocks; gate/up
-      // +2.0 % on the Llama3-8x70B training step). dH keeps one N tile and
-      // its overlapped epilogue (A_save loads and the SwiGLU backward): on
-      // that step it measured 1.1 % faster than two tiles
-      if constexpr (MODE == DOWN || MODE == DX)
+      // down projection, dXp and dH with K >= 8192 (128 K blocks), gate/up
+      // with K >= 4096. Measured A/B on one box: gate/up +2.0 % on the
+      // Llama3-8x70B training step (K = 8192), +2.2 % on the Mixtral-8x22B
+      // forward and +1.0 % on the G8T8 step (K = 6144); dH +0.8 % on the
+      // Llama3 step (it lost 1.1 % there while its sigmoid took a correctly
+      // rounded reciprocal, when its epilogue was twice as long)
+      if constexpr (MODE == DOWN || MODE == DX || MODE == DH)
         if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192)
           return launch_pair_and_tails<MODE, 256, 2>(p, s);
       if constexpr (MODE == GU)
-        if ((p.N / 128) % 2 == 0 && p.K_fixed >= 8192)
+        if ((p.N / 128) % 2 == 0 && p.K_fixed >= 4096)
           return launch_pair_and_tails<GU, 128, 2>(p, s);
       if constexpr (red)   // K = a group's rows: the same test on the mean rows per group
         if (bn256 && (p.N / 256) % 2 == 0 && p.max_rows / p.n_groups >= 8192)
