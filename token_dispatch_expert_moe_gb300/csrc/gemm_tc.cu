@@ -1643,14 +1643,16 @@ cudaError_t launch_bn(const TcParams &p, cudaStream_t s) {
     if (pair_enabled() && (!red || p.M_fixed % 256 == 0)) {
       // two N tiles per pair tile where the epilogue (no longer overlapped
       // with the next tile's mainloop) is short against a long K loop: the
-      // down projection, dXp and dH with K >= 8192 (128 K blocks), gate/up
-      // with K >= 4096. Measured A/B on one box: gate/up +2.0 % on the
-      // Llama3-8x70B training step (K = 8192), +2.2 % on the Mixtral-8x22B
-      // forward and +1.0 % on the G8T8 step (K = 6144); dH +0.8 % on the
-      // Llama3 step (it lost 1.1 % there while its sigmoid took a correctly
-      // rounded reciprocal, when its epilogue was twice as long)
+      // down projection and dH with K >= 8192 (128 K blocks), dXp and
+      // gate/up with K >= 4096. Measured A/B on one box: gate/up +2.0 % on
+      // the Llama3-8x70B training step (K = 8192), +2.2 % on the
+      // Mixtral-8x22B forward and +1.0 % on the G8T8 step (K = 6144), no gain
+      // at K = 3584; dH +0.8 % on the Llama3 step (it lost 1.1 % there while
+      // its sigmoid took a correctly rounded reciprocal) and a loss of 1 %
+      // at K = 3584 and 6144; dXp's backward GEMMs -0.5 to -1.2 % at
+      // K = 4096 and 5120
       if constexpr (MODE == DOWN || MODE == DX || MODE == DH)
-        if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= 8192)
+        if (bn256 && (p.N / 256) % 2 == 0 && p.K_fixed >= (MODE == DX ? 4096 : 8192))
           return launch_pair_and_tails<MODE, 256, 2>(p, s);
       if constexpr (MODE == GU)
         if ((p.N / 128) % 2 == 0 && p.K_fixed >= 4096)
