@@ -234,6 +234,20 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Four rows of a tensor map whose box is one row high (tile::gather4): rows
+// r0..r3, columns c0 .. c0 + box width, put one after another at dst in this
+// CTA's shared memory; completes on a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap *tm,
+                                                 uint32_t bar_cluster, int c0, int r0, int r1,
+                                                 int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar_cluster), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3)
+      : "memory");
+}
+
 // TMA load into this CTA's shared memory that completes on a barrier of
 // either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *tm,
@@ -1121,7 +1135,7 @@ template <int MODE, int BN, int NSUB, bool GATHER>
 __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(MODE != RT, "the router GEMM runs single-CTA");
-  static_assert(!GATHER || (MODE == GU && NSUB == 1), "the A gather serves the gate/up GEMM");
+  static_assert(!GATHER || MODE == GU, "the A gather serves the gate/up GEMM");
   using TR = ModeTraits<MODE>;
   constexpr int kPairStages = pair_stages<NSUB>();
   constexpr int kPairStageBytes = pair_stage_bytes<NSUB>();
@@ -1370,29 +1384,30 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
     __syncwarp();
   } else if constexpr (GATHER) {
     // ==================== A gather (GU, both CTAs) ====================
-    // Lane l of gather warp w loads rows r = 64 w + 2 l and r + 1 of this
-    // CTA's 128-row A box: per stage one TMA copy per row, a box of one row
-    // and 64 columns of x (128 bytes) put at byte offset 128 r of the stage,
-    // which is where the 128-byte swizzled box the MMA descriptor reads keeps
-    // row r (the swizzle is anchored to the shared-memory address, and the
-    // stage is 1024-byte aligned). A row without a source (past the last
-    // group, or a padding row) loads row -1: outside x, so the copy fills
-    // zeros. The copies complete on the even CTA's full barrier, on which
-    // lane 0 first arrives with the warp's 64 rows of bytes; the TMA
-    // completion orders the writes for the tensor core.
-    constexpr int kRows = BM / (32 * kGatherWarps);   // 2 rows per lane
+    // Lane l < 16 of gather warp w loads rows r = 64 w + 4 l .. r + 3 of this
+    // CTA's 128-row A box: per stage one tile::gather4 copy, four boxes of
+    // one row and 64 columns of x (128 bytes each) put at byte offset 128 r
+    // of the stage, one after another, which is where the 128-byte swizzled
+    // box the MMA descriptor reads keeps rows r .. r + 3 (the swizzle is
+    // anchored to the shared-memory address, and the stage is 1024-byte
+    // aligned). A row without a source (past the last group, or a padding
+    // row) loads row -1: outside x, so the copy fills zeros. The copies
+    // complete on the even CTA's full barrier, on which lane 0 first arrives
+    // with the warp's 64 rows of bytes; the TMA completion orders the writes
+    // for the tensor core.
+    constexpr int kLanes = BM / (4 * kGatherWarps);   // 16 lanes of 4 rows per warp
     const int gw = warp - 6;
     const int64_t n_rows = p.offsets[p.n_groups];
     const int64_t n_src = p.gT * p.gK;
     int it = 0;
     for (int pt = cid; pt < total && !st.abort; pt += ncl) {
       const Tile t = decode_pair_tile<MODE, BN, NSUB>(p, st, pt, (int)rank);
-      int tok[kRows];
+      int tok[4];
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) {
-        const int64_t R = (int64_t)t.row0 + (int64_t)t.m * BM + 64 * gw + 2 * lane + j;
+      for (int j = 0; j < 4; ++j) {
+        const int64_t R = (int64_t)t.row0 + (int64_t)t.m * BM + 64 * gw + 4 * lane + j;
         tok[j] = -1;
-        if (R < n_rows) {
+        if (lane < kLanes && R < n_rows) {
           const int32_t so = p.src_of[R];
           if (so >= 0 && so < n_src) tok[j] = so / p.gK;
           else if (so >= 0) report(p.status, MOE_ERR_DEVICE, kInfoRowRange);
@@ -1407,15 +1422,16 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
         bool w = true;
         if (lane == 0) {
           w = wait_bounded(st, smem_u32(&st.empty[s]), ph ^ 1, p.status, 6);
-          if (w) mbar_arrive_expect_tx_cluster(bar, 32 * kRows * 128);
+          if (w) mbar_arrive_expect_tx_cluster(bar, 4 * kLanes * 128);
         }
         if (!__shfl_sync(0xffffffffu, w, 0)) {
           ok = false;
           break;
         }
-        const uint32_t dst = smem_u32(smem + s * kPairStageBytes) + (64 * gw + 2 * lane) * 128;
-#pragma unroll
-        for (int j = 0; j < kRows; ++j) tma_load_2d_pair(dst + j * 128, &p.tmX, bar, kb * BK, tok[j]);
+        if (lane < kLanes) {
+          const uint32_t dst = smem_u32(smem + s * kPairStageBytes) + (64 * gw + 4 * lane) * 128;
+          tma_gather4_pair(dst, &p.tmX, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
+        }
       }
       if (!ok) break;
     }
@@ -1747,10 +1763,16 @@ cudaError_t launch_ffn_fwd_bf16(const FfnArgs &a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (gather) {
-    // one-row boxes of x: the gather warps load each permuted row by itself
+    // one-row boxes of x: the gather warps load the permuted rows four at a
+    // time (tile::gather4); two N tiles per pair tile under the same rule as
+    // the gate/up GEMM fed by Xp, so that each gathered A stage serves twice
+    // the MMA work
     if (!make_map(&p.tmX, a.x, d, (uint64_t)a.T, 1)) return cudaErrorInvalidValue;
     p.src_of = a.src_of; p.gK = a.K; p.gT = a.T;
-    e = launch_pair<GU, 128, 1, true>(p, s);
+    if (pair_enabled() && (p.N / 128) % 2 == 0 && p.K_fixed >= 4096)
+      e = launch_pair<GU, 128, 2, true>(p, s);
+    else
+      e = launch_pair<GU, 128, 1, true>(p, s);
   } else {
     e = launch_bn<GU>(p, s);
   }
