@@ -613,9 +613,27 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
     if (!valid) return;
     if (p.ep == 0) {   // logits only: the Top-K kernel routes
       float *lg = reinterpret_cast<float *>(p.out0) + row * p.E;
+      if ((p.E & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out0) & 15) == 0) {
+        // four logits per 16-byte store: a thread writes its own row, so a
+        // warp's store touches 32 rows; wide stores cut those transactions 4x
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[e], p.bias[e]) : v[e];
+        for (int e = 0; e < NV; e += 4) {
+          if (e < p.E) {
+            float4 w = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            if (p.bias != nullptr) {
+              w.x = __fadd_rn(w.x, p.bias[e]);
+              w.y = __fadd_rn(w.y, p.bias[e + 1]);
+              w.z = __fadd_rn(w.z, p.bias[e + 2]);
+              w.w = __fadd_rn(w.w, p.bias[e + 3]);
+            }
+            *reinterpret_cast<float4 *>(lg + e) = w;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+          if (e < p.E) lg[e] = p.bias != nullptr ? __fadd_rn(v[e], p.bias[e]) : v[e];
+        }
       }
       if (p.has_gate) p.gate_out[row] = v[GC];
       return;
