@@ -575,6 +575,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
     const int64_t row = r_loc;
     const bool valid = row < p.T;
     const int C = p.E + p.has_gate;
+    const int CS = (C + 3) & ~3;   // exchange row stride (16-byte aligned rows)
+    // the row's values sit in v[0 .. C) already (no gate, or the gate column
+    // right after the experts): the exchange moves them four at a time
+    const bool contig = (p.E & 3) == 0 && (!p.has_gate || GC == p.E);
     float v[NV];
 #pragma unroll
     for (int c = 0; c < NV / 32; ++c) {
@@ -588,12 +592,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
       // others in part order
       if (t.n != 0) {
         if (valid) {
-          const uint32_t dst = map_to_cta(smem_u32(xbuf + ((t.n - 1) * BM + rl) * C), 0);
+          const uint32_t dst = map_to_cta(smem_u32(xbuf + ((t.n - 1) * BM + rl) * CS), 0);
+          if (contig) {
 #pragma unroll
-          for (int j = 0; j < NV; ++j) {
-            const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
-            if (e >= 0)
-              asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * e), "f"(v[j]) : "memory");
+            for (int j = 0; j < NV; j += 4)
+              if (j < CS)
+                asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 4 * j),
+                             "f"(v[j]), "f"(v[j + 1]), "f"(v[j + 2]), "f"(v[j + 3])
+                             : "memory");
+          } else {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+              const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
+              if (e >= 0)
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst + 4 * e), "f"(v[j]) : "memory");
+            }
           }
         }
         mbar_arrive_cluster(map_to_cta(smem_u32(&st.xbar), 0));
@@ -602,11 +615,24 @@ __device__ __forceinline__ void epilogue_tile(const TcParams &p, SharedState &st
       if (!wait_bounded(st, smem_u32(&st.xbar), 0, p.status, 7, true)) return;
       if (!valid) return;
       for (int part = 1; part < p.k_split; ++part) {
-        const float *src = xbuf + ((part - 1) * BM + rl) * C;
+        const float *src = xbuf + ((part - 1) * BM + rl) * CS;
+        if (contig) {
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
-          if (e >= 0) v[j] = __fadd_rn(v[j], src[e]);
+          for (int j = 0; j < NV; j += 4) {
+            if (j < CS) {
+              const float4 w = *reinterpret_cast<const float4 *>(src + j);
+              v[j] = __fadd_rn(v[j], w.x);
+              v[j + 1] = __fadd_rn(v[j + 1], w.y);
+              v[j + 2] = __fadd_rn(v[j + 2], w.z);
+              v[j + 3] = __fadd_rn(v[j + 3], w.w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NV; ++j) {
+            const int e = j < p.E ? j : (j == GC && p.has_gate ? p.E : -1);
+            if (e >= 0) v[j] = __fadd_rn(v[j], src[e]);
+          }
         }
       }
     }
@@ -1722,7 +1748,9 @@ int router_parts(int64_t T, int d, int E, int has_gate) {
   const int n = (E + 15) / 16 * 16 + 16 * has_gate;
   const size_t stage = kABytes + ((size_t)n * BK * 2 + 1023) / 1024 * 1024;
   const size_t room = (size_t)kStages * kStageBytes + kEpiStagingBytes - 6 * stage;
-  const int max_parts = 1 + (int)(room / ((size_t)BM * (E + has_gate) * sizeof(float)));
+  // each part's partial sums: BM rows of E (+ gate) floats, the row stride
+  // rounded up to 4 floats
+  const int max_parts = 1 + (int)(room / ((size_t)BM * ((E + has_gate + 3) & ~3) * sizeof(float)));
   const int split = router_k_split(T, d);
   return split < max_parts ? split : max_parts;
 }
