@@ -67,6 +67,25 @@ def test_ffn_group_layouts(rows, dtype):
     _check_fwd(L, dtype, Xp, offsets, W_gu, W_down, d, F)
 
 
+@pytest.mark.parametrize("rows,d,F", [
+    ([300, 129, 1, 0, 700], 4096, 256),   # gate/up with K = d = 4096 (two N tiles per pair tile)
+    ([300, 0, 200], 512, 8192),           # down projection with K = F = 8192 (two N tiles)
+])
+def test_ffn_forward_long_k(rows, d, F):
+    """The forward shapes that switch the gate/up and down GEMMs to two N
+    tiles per pair tile, on ragged groups (a one-row group, an empty one, last
+    tiles of at most 128 rows for the tail kernel), every element against the
+    oracle."""
+    L = lib()
+    G = len(rows)
+    offsets = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    n = int(offsets[-1])
+    Xp = normal_bf16(8, 101, (n, d))
+    W_gu = normal_bf16(8, 102, (G, 2 * F, d), 1 / np.sqrt(d))
+    W_down = normal_bf16(8, 103, (G, d, F), 1 / np.sqrt(F))
+    _check_fwd(L, "bf16", Xp, offsets, W_gu, W_down, d, F)
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_ffn_forward_full_size_sampled(name):
     """Full-size grouped GEMM on the workload's routing; 3 sampled rows per
@@ -149,6 +168,7 @@ def test_single_cta_and_pair_kernels_agree(pair):
     ([8300, 8100], 512, 512),   # weight gradients: >= 8192 rows per group (two N tiles per pair tile)
     ([300, 0, 200], 8192, 512),  # dH with K = d = 8192 (two N tiles per pair tile)
     ([300, 200], 512, 4096),     # dXp with K = 2F = 8192 (two N tiles per pair tile)
+    ([300, 129, 1], 512, 2048),  # dXp at the two-tile threshold, K = 2F = 4096, with tail tiles
 ])
 def test_ffn_backward_long_k(rows, d, F):
     """The long-K shapes that switch the CTA-pair GEMMs to two N tiles per

@@ -101,6 +101,11 @@ SPLIT_K = {
     "split4_gate_bias": ("qwen2_57b_a14b", dict(T=1000, d=2048, F=128, Fs=128)),
     "split3_ragged": ("mixtral_8x22b", dict(T=300, d=1536, F=128, S=100)),
     "split2_e64": ("mixtral_8x22b_g8t8", dict(T=2000, d=1024, F=128, S=500)),
+    # the exchange and logits paths for rows that are not four contiguous
+    # floats at a time: the gate column away from the experts (E = 8 padded
+    # to 16), and E = 9
+    "split4_gate_e8": ("qwen2_57b_a14b", dict(T=1000, d=2048, F=128, E=8, K=2, Fs=128)),
+    "split4_e9": ("mixtral_8x22b", dict(T=1000, d=2048, F=128, E=9, S=250)),
 }
 
 
