@@ -1343,16 +1343,65 @@ __global__ void __launch_bounds__(GATHER ? kThreadsGather : kThreads, 1)
         // every tile uses both (buffer j for its j-th N tile)
         const int buf = NSUB == 1 ? (tcount & 1) : 0;
         const uint32_t use = NSUB == 1 ? ((tcount >> 1) & 1) : (tcount & 1);
-        bool waited = true;
-#pragma unroll
-        for (int j = 0; j < NSUB; ++j)
-          waited = waited && __all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf + j]),
-                                                                  use ^ 1, p.status, 2));
-        if (!waited) break;
+        // NSUB = 2: the epilogue drains the tile's two accumulators in order,
+        // so accumulator 0's MMAs for the stages already loaded (up to the
+        // ring's depth) go ahead while accumulator 1 is still being read; then
+        // accumulator 1's MMAs for those stages, which releases them
+        const int look = NSUB == 2 ? min(kblocks, kPairStages) : 0;
+        if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf]), use ^ 1, p.status, 2)))
+          break;
         tc_fence_after();
         const uint32_t dcol = tmem + buf * 256;
         bool ok = true;
-        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        if constexpr (NSUB == 2) {
+          for (int kb = 0; kb < look; ++kb) {
+            const int s = (it + kb) % kPairStages;
+            const uint32_t ph = ((it + kb) / kPairStages) & 1;
+            if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
+              const uint32_t sb = sa + kABytes;
+#pragma unroll
+              for (int ks = 0; ks < BK / 16; ++ks) {
+                uint64_t ad, bd;
+                if constexpr (TR::a_mn) ad = smem_desc(sa + ks * 2048, 8192, 1024);
+                else ad = smem_desc(sa + ks * 32, 16, 1024);
+                if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
+                else bd = smem_desc(sb + ks * 32, 16, 1024);
+                tc_mma_pair(dcol, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+              }
+            }
+            __syncwarp();
+          }
+          if (!ok) break;
+          if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.tempty[buf + 1]), use ^ 1, p.status, 2)))
+            break;
+          tc_fence_after();
+          for (int kb = 0; kb < look; ++kb, ++it) {
+            const int s = it % kPairStages;
+            if (lane == 0) {
+              const uint32_t sa = smem_u32(smem + s * kPairStageBytes);
+              const uint32_t sb = sa + kABytes + 16384;
+#pragma unroll
+              for (int ks = 0; ks < BK / 16; ++ks) {
+                uint64_t ad, bd;
+                if constexpr (TR::a_mn) ad = smem_desc(sa + ks * 2048, 8192, 1024);
+                else ad = smem_desc(sa + ks * 32, 16, 1024);
+                if constexpr (TR::b_mn) bd = smem_desc(sb + ks * 2048, 8192, 1024);
+                else bd = smem_desc(sb + ks * 32, 16, 1024);
+                tc_mma_pair(dcol + 256, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+              }
+              tc_commit_pair_both(smem_u32(&st.empty[s]));
+              issued_any = true;
+            }
+            __syncwarp();
+          }
+        }
+        for (int kb = look; kb < kblocks; ++kb, ++it) {
           const int s = it % kPairStages;
           const uint32_t ph = (it / kPairStages) & 1;
           if (!__all_sync(0xffffffffu, wait_bounded(st, smem_u32(&st.full[s]), ph, p.status, 3))) {
