@@ -16,13 +16,19 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane
 //               quarter per warp), fused math, 32-row slabs staged in swizzled
 //               shared memory and written with TMA bulk stores.
-// tc_gemm_kernel: one CTA per tile, M = 128, 4 stages of 48 KB (6 of 32 KB in
-// the router mode; used by the router GEMM and when CTA pairs are disabled). tc_gemm_pair_kernel: clusters
-// of two CTAs on one TPC issue tcgen05.mma.cta_group::2 (M = 256, each CTA
-// holding its 128 rows of A and half of B), 6 stages of 32 KB per CTA; the
-// even CTA's barriers see both CTAs' TMA bytes and its MMA warp issues for the
-// pair. Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile
-// overlap the mainloop of the next.
+// tc_gemm_kernel: one CTA per tile, M = 128, 4 stages of 48 KB (6 smaller
+// ones in the router mode); it runs the router GEMM, the row-grouped experts'
+// last tiles of at most 128 rows (as a programmatic dependent of the pair
+// kernel), and every tile when CTA pairs are disabled. tc_gemm_pair_kernel:
+// clusters of two CTAs on one TPC issue tcgen05.mma.cta_group::2 (M = 256,
+// each CTA holding its 128 rows of A and half of B), 6 stages of 32 KB per
+// CTA; the even CTA's barriers see both CTAs' TMA bytes and its MMA warp
+// issues for the pair. Two TMEM accumulators (2 x 256 columns) let the
+// epilogue of one tile overlap the mainloop of the next; where K is long, a
+// pair tile covers two adjacent N tiles instead (4 stages of 48 KB sharing
+// each A box, one accumulator per N tile), and the MMA warp starts a tile's
+// accumulator 0 as soon as the epilogue has drained it. In the gate/up mode
+// with the permutation fused in, two more warps gather the A rows from x.
 //
 // The GEMMs (A: M x K, B: N x K, per group g):
 //   GU      [G|U] = Xp W_gu[g]^T, SwiGLU epilogue H = silu(G) U (+ A_save)
@@ -35,8 +41,10 @@
 //           group of T rows, N = E rounded up to 16 (+ 16 when the gate
 //           vector rides along as a second B box); fp32 logits out. When
 //           T / 128 row tiles would leave SMs idle, the K loop is split over
-//           k_split tiles per row tile whose fp32 partial sums the Top-K
-//           kernel adds in split order.
+//           a cluster of k_split CTAs per row tile: the odd CTAs send their
+//           fp32 partial sums to the even CTA's shared memory, which adds them
+//           in part order. With no split and E <= 16 the epilogue also routes
+//           (softmax, Top-K, combine weights).
 // In GU/DOWN/DH/DX a tile's rows past the group's end belong to the next
 // group (or are zero-filled past the buffer); only their outputs are masked.
 // In WGD/WGU the reduction runs over the group's rows: the loads go through
