@@ -6,13 +6,14 @@
 // decided inside each sub-sequence; sub-sequence dropping is the default).
 //
 // bf16 layers compute the logits (and the shared-expert gate logit) on the
-// tensor cores (router mode of the grouped GEMM, gemm_tc.cu; with a split K
-// loop when T / 128 row tiles would leave SMs idle) and then run
-// topk_from_logits_kernel, which also adds the split partial sums and the
-// bias; fp32 layers use router_fused_kernel, which does the logits GEMV,
-// softmax and Top-K in one pass. capacity_kernel applies the drop rule per
-// (sub-sequence, expert). The softmax and Top-K arithmetic is
-// specified in softmax.cuh.
+// tensor cores (router mode of the grouped GEMM, gemm_tc.cu, which adds the
+// bias; its K loop split over a cluster of CTAs when T / 128 row tiles would
+// leave SMs idle). With E <= 16 and no split that kernel's epilogue also
+// routes; otherwise topk_from_logits_kernel does, a warp per token. fp32
+// layers use router_fused_kernel, which does the logits GEMV, softmax and
+// Top-K in one pass. capacity_bucket_kernel and capacity_select_kernel apply
+// the drop rule per (sub-sequence, expert). The softmax and Top-K arithmetic
+// is specified in softmax.cuh.
 #include "common.cuh"
 #include "softmax.cuh"
 
